@@ -1,0 +1,131 @@
+/*
+ * Oracle for C = ReLU(A . B) -- TEST INFRASTRUCTURE ONLY.
+ *
+ * This file is the slow, obviously-correct CPU definition that the CUDA
+ * path is checked against.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load it; the product library never
+ * links, calls or falls back to it.  It shares no code, header, table or
+ * helper with the CUDA sources.
+ *
+ * What it computes (the GEMM+ReLU worked example of "Writing
+ * High-Performance Kernels in TileLang", atlascloud.ai guide, section
+ * "Vamos escrever um GEMM" / its Korean twin, listing `matmul_relu_kernel`):
+ *   - the accumulator tile is cleared,
+ *   - A(M,K) . B(K,N) is accumulated over the whole K range,
+ *   - ReLU (max with 0) is applied to the accumulator,
+ *   - the result is written to C(M,N).
+ * A and B are row-major IEEE binary16, C is returned in binary64 and is
+ * NOT rounded to binary16: the comparison tolerance absorbs that rounding.
+ *
+ * Readings taken where the pages are silent:
+ *   - accumulation is in binary64 (stronger than the pages' fp32), loop
+ *     order i-k-j, so for every (i,j) the terms are added in k order;
+ *   - ReLU maps -0.0 to +0.0 (max(x, 0) with the sign of zero dropped);
+ *   - NaN/Inf inputs are not part of the contract (parity unpinned there).
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <math.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Exact binary16 -> binary64 decode, from the IEEE 754 bit layout:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_half_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int exp = (h >> 10) & 0x1f;
+    const int frac = h & 0x3ff;
+    double v;
+    if (exp == 0) {
+        /* zero or subnormal: frac * 2^-24 */
+        v = ldexp((double)frac, -24);
+    } else if (exp == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        /* normal: (1024 + frac) * 2^(exp - 15 - 10) */
+        v = ldexp((double)(1024 + frac), exp - 25);
+    }
+    return sign ? -v : v;
+}
+
+static void decode_all(const uint16_t* src, double* dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) dst[i] = oracle_half_to_double(src[i]);
+}
+
+static double relu(double x)
+{
+    return x > 0.0 ? x : 0.0; /* also turns -0.0 into +0.0 */
+}
+
+/*
+ * Full product.  A: M x K, B: K x N, C: M x N (binary64, caller-owned).
+ * Ad/Bd are caller-provided binary64 scratch of M*K and K*N entries.
+ * num_threads <= 0 uses one thread.  Rows are independent, so splitting
+ * them over threads does not change any result bit.
+ * Returns 0 on success, -1 on bad arguments.
+ */
+int oracle_gemm_relu(const uint16_t* A, const uint16_t* B, double* C,
+                     int64_t M, int64_t N, int64_t K, int apply_relu,
+                     double* Ad, double* Bd, int num_threads)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if ((M && N && K) && (!A || !B || !Ad || !Bd)) return -1;
+    if (M && N && !C) return -1;
+    decode_all(A, Ad, M * K);
+    decode_all(B, Bd, K * N);
+    if (num_threads < 1) num_threads = 1;
+    int64_t i;
+#pragma omp parallel for num_threads(num_threads) schedule(static)
+    for (i = 0; i < M; ++i) {
+        double* crow = C + i * N;
+        for (int64_t j = 0; j < N; ++j) crow[j] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = Ad[i * K + k];
+            const double* brow = Bd + k * N;
+            for (int64_t j = 0; j < N; ++j) crow[j] += a * brow[j];
+        }
+        if (apply_relu)
+            for (int64_t j = 0; j < N; ++j) crow[j] = relu(crow[j]);
+    }
+    return 0;
+}
+
+/*
+ * Selected outputs only: out[t] = (ReLU)(sum_k A[rows[t],k] * B[k,cols[t]]),
+ * summed in k order, exactly as the full product above does for that entry.
+ * Used to check full-size problems at sampled positions.
+ */
+int oracle_gemm_relu_entries(const uint16_t* A, const uint16_t* B,
+                             int64_t M, int64_t N, int64_t K, int apply_relu,
+                             const int64_t* rows, const int64_t* cols,
+                             int64_t count, double* out, int num_threads)
+{
+    if (M < 0 || N < 0 || K < 0 || count < 0) return -1;
+    if (num_threads < 1) num_threads = 1;
+    for (int64_t t = 0; t < count; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+    int64_t t;
+#pragma omp parallel for num_threads(num_threads) schedule(static)
+    for (t = 0; t < count; ++t) {
+        const int64_t i = rows[t], j = cols[t];
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += oracle_half_to_double(A[i * K + k]) *
+                   oracle_half_to_double(B[k * N + j]);
+        out[t] = apply_relu ? relu(acc) : acc;
+    }
+    return 0;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

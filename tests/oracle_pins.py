@@ -1,0 +1,188 @@
+"""Checks that pin the CPU oracle to facts outside itself (test helper).
+
+Each ``pin_*`` function takes a reference callable
+``ref(A16, B16, apply_relu) -> float64 (M, N) array`` and returns a list of
+failure messages (empty when the callable passes).  They are run against
+the real oracle (all must pass) and against deliberately broken variants of
+it (each variant must fail at least one), which shows the pins can see the
+mistakes they are meant to catch.
+
+What fixes the expected values, none of it the oracle's own code:
+* hand-worked fixtures (tests/golden), exact rationals;
+* brute force in exact rational arithmetic (``fractions``) on tiny inputs,
+  with binary16 values decoded by numpy;
+* integer inputs whose products and sums are exact in every format,
+  checked against numpy int64 matmul;
+* closed forms: identity B gives ReLU(A), all-ones A gives ReLU of B's
+  column sums;
+* invariants: ReLU output non-negative with no -0; zero K-padding changes
+  nothing; relu-off is odd in A and homogeneous in B; relu-on equals
+  max(relu-off, 0); (A.B)^T equals B^T.A^T;
+* a float64 matmul from a library (torch CPU) within the binary64 bound.
+"""
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from golden_io import all_fixtures
+
+U64 = 2.0 ** -53  # unit roundoff of binary64
+
+
+def _h(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+
+def _frac(x):
+    """Exact rational value of a finite float; None for inf/NaN."""
+    x = float(x)
+    return Fraction(x) if np.isfinite(x) else None
+
+
+def _exact_product(A16, B16):
+    """Exact rational A.B (lists of Fractions) from binary16 inputs."""
+    Af = [[Fraction(float(v)) for v in row] for row in A16.astype(np.float64)]
+    Bf = [[Fraction(float(v)) for v in row] for row in B16.astype(np.float64)]
+    M, K = len(Af), len(Bf)
+    N = B16.shape[1]
+    return [[sum((Af[i][k] * Bf[k][j] for k in range(K)), Fraction(0)) for j in range(N)]
+            for i in range(M)]
+
+
+def _bound(A16, B16):
+    """gamma_K * |A|.|B| : a rigorous bound on binary64 accumulation error."""
+    K = A16.shape[1]
+    gk = K * U64 / (1 - K * U64) if K else 0.0
+    return gk * (np.abs(A16.astype(np.float64)) @ np.abs(B16.astype(np.float64)))
+
+
+def pin_golden(ref):
+    fails = []
+    for fx in all_fixtures():
+        for relu, key in ((True, "C_relu"), (False, "C_norelu")):
+            got = ref(fx["A"], fx["B"], relu)
+            exp = fx[key]
+            for i, row in enumerate(exp):
+                for j, e in enumerate(row):
+                    if _frac(got[i, j]) != e:
+                        fails.append(f"golden {fx['name']} relu={relu} [{i},{j}]: {got[i, j]} != {e}")
+    return fails
+
+
+def pin_bruteforce(ref, trials=40, seed=123):
+    rng = np.random.default_rng(seed)
+    fails = []
+    for t in range(trials):
+        M, N, K = (int(x) for x in rng.integers(1, 8, size=3))
+        A = _h(rng.standard_normal((M, K)) * 3)
+        B = _h(rng.standard_normal((K, N)) * 3)
+        exact = _exact_product(A, B)
+        bnd = _bound(A, B)
+        for relu in (True, False):
+            got = ref(A, B, relu)
+            for i in range(M):
+                for j in range(N):
+                    e = exact[i][j]
+                    if relu:
+                        e = max(e, Fraction(0))
+                    g = _frac(got[i, j])
+                    if g is None or abs(g - e) > Fraction(float(bnd[i, j])):
+                        fails.append(f"bruteforce t={t} ({M},{N},{K}) relu={relu} [{i},{j}]: "
+                                     f"{got[i, j]!r} vs {float(e)!r}")
+    return fails
+
+
+def pin_integer_exact(ref, seed=7):
+    rng = np.random.default_rng(seed)
+    M, N, K = 33, 47, 300
+    Ai = rng.integers(-2, 3, size=(M, K))
+    Bi = rng.integers(-2, 3, size=(K, N))
+    exact = Ai.astype(np.int64) @ Bi.astype(np.int64)
+    fails = []
+    for relu in (True, False):
+        got = ref(_h(Ai), _h(Bi), relu)
+        exp = np.maximum(exact, 0) if relu else exact
+        if not np.array_equal(got, exp.astype(np.float64)):
+            bad = np.argwhere(got != exp)
+            fails.append(f"integer relu={relu}: {len(bad)} mismatches, first {bad[0].tolist()}")
+    return fails
+
+
+def pin_identity(ref, seed=11):
+    rng = np.random.default_rng(seed)
+    M, K = 9, 13
+    A = _h(rng.standard_normal((M, K)))
+    I = _h(np.eye(K))
+    got = ref(A, I, True)
+    exp = np.maximum(A.astype(np.float64), 0.0)
+    return [] if np.array_equal(got, exp) else ["identity B did not give ReLU(A)"]
+
+
+def pin_ones(ref, seed=12):
+    rng = np.random.default_rng(seed)
+    M, N, K = 4, 10, 12
+    Ai = np.ones((M, K))
+    B = _h(rng.standard_normal((K, N)))
+    fails = []
+    colsum = [sum((Fraction(float(B[k, j])) for k in range(K)), Fraction(0)) for j in range(N)]
+    bnd = _bound(_h(Ai), B)
+    got = ref(_h(Ai), B, True)
+    for i in range(M):
+        for j in range(N):
+            e = max(colsum[j], Fraction(0))
+            g = _frac(got[i, j])
+            if g is None or abs(g - e) > Fraction(float(bnd[i, j])):
+                fails.append(f"all-ones A [{i},{j}]: {got[i, j]} vs {float(e)}")
+    return fails
+
+
+def pin_invariants(ref, seed=13):
+    rng = np.random.default_rng(seed)
+    fails = []
+    M, N, K = 17, 23, 29
+    A = _h(rng.standard_normal((M, K)))
+    B = _h(rng.standard_normal((K, N)))
+    on = ref(A, B, True)
+    off = ref(A, B, False)
+    if (on < 0).any() or np.signbit(on).any():
+        fails.append("ReLU output has negatives or -0")
+    if not np.array_equal(on, np.where(off > 0, off, 0.0)):
+        fails.append("relu-on != max(relu-off, 0)")
+    # zero K padding
+    Ap = np.concatenate([A, np.zeros((M, 7), np.float16)], axis=1)
+    Bp = np.concatenate([B, np.zeros((7, N), np.float16)], axis=0)
+    if not np.array_equal(ref(Ap, Bp, False), off):
+        fails.append("zero K-tail changed the result")
+    # odd in A, homogeneous in B (scaling by 2 is exact in both formats)
+    if not np.array_equal(ref(-A, B, False), -off):
+        fails.append("relu-off not odd in A")
+    if not np.array_equal(ref(A, _h(B.astype(np.float64) * 2), False), 2 * off):
+        fails.append("relu-off not homogeneous in B")
+    # transpose: (A.B)^T == B^T.A^T (same k order per entry => bit-identical)
+    if not np.array_equal(ref(np.ascontiguousarray(B.T), np.ascontiguousarray(A.T), False), off.T):
+        fails.append("(A.B)^T != B^T.A^T")
+    return fails
+
+
+def pin_torch64(ref, seed=14):
+    rng = np.random.default_rng(seed)
+    M, N, K = 40, 50, 300
+    A = _h(rng.standard_normal((M, K)))
+    B = _h(rng.standard_normal((K, N)))
+    lib = (torch.from_numpy(A.astype(np.float64)) @ torch.from_numpy(B.astype(np.float64))).numpy()
+    bnd = 2 * _bound(A, B)  # both sides round in binary64, orders may differ
+    fails = []
+    for relu in (True, False):
+        exp = np.maximum(lib, 0) if relu else lib
+        got = ref(A, B, relu)
+        if not (np.abs(got - exp) <= bnd).all():
+            fails.append(f"torch float64 matmul disagrees (relu={relu}), "
+                         f"max err {np.abs(got - exp).max():.3e}")
+    return fails
+
+
+ALL_PINS = [pin_golden, pin_bruteforce, pin_integer_exact, pin_identity, pin_ones,
+            pin_invariants, pin_torch64]

@@ -1,0 +1,130 @@
+"""The CPU oracle against its pins, and the pins against planted mistakes.
+
+CPU only (no GPU, no CUDA library).  The planted mistakes are made in the
+oracle, on the CPU: each mutant wraps the real oracle with one plausible
+bug, and at least one pin must reject it.
+"""
+import numpy as np
+import pytest
+
+import oracle_pins as P
+
+
+def _real(oracle_mod):
+    return lambda A, B, relu: oracle_mod.gemm_relu(A, B, relu)
+
+
+@pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_passes_pin(oracle_mod, pin):
+    fails = pin(_real(oracle_mod))
+    assert not fails, "\n".join(fails[:10])
+
+
+def test_half_decode_matches_ieee(oracle_mod):
+    # spot values from the binary16 definition
+    known = {0x3C00: 1.0, 0xC000: -2.0, 0x7BFF: 65504.0, 0x0001: 2.0 ** -24,
+             0x0400: 2.0 ** -14, 0x03FF: 1023 * 2.0 ** -24, 0x3555: 0.333251953125,
+             0x0000: 0.0, 0x7C00: float("inf"), 0xFC00: float("-inf")}
+    for bits, val in known.items():
+        assert oracle_mod.half_to_double(bits) == val, hex(bits)
+    assert np.signbit(oracle_mod.half_to_double(0x8000))
+    assert np.isnan(oracle_mod.half_to_double(0x7E00))
+    # every finite pattern against numpy's conversion
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_mod.half_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.signbit(got[finite]), np.signbit(ref[finite]))
+
+
+def test_entries_equal_full_product(oracle_mod):
+    rng = np.random.default_rng(5)
+    M, N, K = 37, 41, 130
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    B = rng.standard_normal((K, N)).astype(np.float16)
+    full = oracle_mod.gemm_relu(A, B, True)
+    rows = rng.integers(0, M, 200)
+    cols = rng.integers(0, N, 200)
+    ent = oracle_mod.gemm_relu_entries(A, B, rows, cols, True)
+    assert np.array_equal(ent, full[rows, cols])
+
+
+def test_threads_do_not_change_bits(oracle_mod):
+    rng = np.random.default_rng(6)
+    A = rng.standard_normal((64, 96)).astype(np.float16)
+    B = rng.standard_normal((96, 80)).astype(np.float16)
+    assert np.array_equal(oracle_mod.gemm_relu(A, B, True, threads=1),
+                          oracle_mod.gemm_relu(A, B, True, threads=4))
+
+
+def test_degenerate_shapes(oracle_mod):
+    A = np.zeros((3, 0), np.float16)
+    B = np.zeros((0, 5), np.float16)
+    c = oracle_mod.gemm_relu(A, B, True)
+    assert c.shape == (3, 5) and not c.any() and not np.signbit(c).any()
+    assert oracle_mod.gemm_relu(np.zeros((0, 4), np.float16), np.zeros((4, 2), np.float16)).shape == (0, 2)
+
+
+def test_tolerance_rule():
+    # |c - ref| <= 1e-2 + 1e-2 |ref|
+    import oracle
+    ref = np.array([0.0, 1.0, 100.0, -3.0])
+    ok = oracle.within_tolerance(ref + np.array([0.0099, 0.0199, 1.0099, 0.0399]), ref)
+    assert ok.tolist() == [True, True, True, True]
+    bad = oracle.within_tolerance(ref + np.array([0.0101, 0.0201, 1.02, 0.0401]), ref)
+    assert bad.tolist() == [False, False, False, False]
+
+
+# ---- planted mistakes: each must be caught by at least one pin -------------
+
+def _mutants(oracle_mod):
+    g = oracle_mod.gemm_relu
+
+    def drop_last_k(A, B, r):
+        if A.shape[1] <= 1:
+            return np.zeros((A.shape[0], B.shape[1]))
+        return g(np.ascontiguousarray(A[:, :-1]), np.ascontiguousarray(B[:-1, :]), r)
+
+    def transposed_b(A, B, r):  # reads B with the wrong stride
+        return g(A, np.ascontiguousarray(B.T).reshape(B.shape), r)
+
+    def relu_as_min(A, B, r):
+        off = g(A, B, False)
+        return np.minimum(off, 0.0) if r else off
+
+    def relu_ignored(A, B, r):
+        return g(A, B, False)
+
+    def rows_shifted(A, B, r):
+        return np.roll(g(A, B, r), 1, axis=0)
+
+    def wrong_exponent_bias(A, B, r):
+        return g(A, B, r) * 0.25
+
+    def fp16_accumulator(A, B, r):
+        M, K = A.shape
+        acc = np.zeros((M, B.shape[1]), np.float16)
+        for k in range(K):
+            acc = (acc.astype(np.float64) + np.outer(A[:, k].astype(np.float64),
+                                                     B[k].astype(np.float64))).astype(np.float16)
+        out = acc.astype(np.float64)
+        return np.where(out > 0, out, 0.0) if r else out
+
+    def first_term_subtracted(A, B, r):
+        off = g(A, B, False) - 2 * np.outer(A[:, 0].astype(np.float64), B[0].astype(np.float64))
+        return np.where(off > 0, off, 0.0) if r else off
+
+    def negative_zero_kept(A, B, r):
+        off = g(A, B, False)
+        return np.where(off > 0, off, -0.0) if r else off
+
+    return [drop_last_k, transposed_b, relu_as_min, relu_ignored, rows_shifted,
+            wrong_exponent_bias, fp16_accumulator, first_term_subtracted, negative_zero_kept]
+
+
+@pytest.mark.parametrize("idx", range(9))
+def test_pins_catch_planted_mistake(oracle_mod, idx):
+    mutant = _mutants(oracle_mod)[idx]
+    caught = [pin.__name__ for pin in P.ALL_PINS if pin(mutant)]
+    assert caught, f"no pin caught the planted mistake {mutant.__name__}"

@@ -1,0 +1,16 @@
+"""GB300-native C = ReLU(A . B): fp16 inputs, fp32 accumulation, fp16 output.
+
+The compute path is a hand-written sm_103a CUDA library behind a C ABI
+(``include/gemm_relu.h``); ``binding`` marshals torch tensors to it.  The
+library is loaded lazily on first use so that importing this package (for
+example to draw the seeded workloads in ``workloads``) needs no GPU.
+"""
+
+__all__ = ["gemm_relu", "workloads"]
+
+
+def __getattr__(name):
+    if name in ("gemm_relu", "gemm_relu_host", "binding"):
+        from . import binding
+        return binding if name == "binding" else getattr(binding, name)
+    raise AttributeError(name)
