@@ -1,0 +1,141 @@
+/*
+ * gemm_relu -- C = ReLU(A . B) on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the GEMM+ReLU worked example of "Writing
+ * High-Performance Kernels in TileLang" (atlascloud.ai guide, GEMM section,
+ * listing `matmul_relu_kernel`; the same listing appears in the CSDN
+ * TileLang note and the Korean edition of the guide):
+ *   A is (M, K), B is (K, N), C is (M, N), all row-major IEEE binary16;
+ *   products are accumulated in binary32 over the whole K range; ReLU,
+ *   max(x, 0), is applied to the binary32 accumulator; the result is rounded
+ *   to binary16 (round-to-nearest-even) and stored.  A ReLU result of zero
+ *   is stored as +0.
+ * The listing's correctness check is assert_close(c, relu(a @ b)) with
+ * rtol = atol = 1e-2, which is the tolerance this library is tested to.
+ *
+ * All functions return a gemm_status_t value and never abort the process.
+ * Device functions use the CUDA device that is current on the calling
+ * thread.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ * default stream); it is declared void* so this header needs no CUDA
+ * headers.
+ */
+#ifndef GEMM_RELU_H
+#define GEMM_RELU_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,        /* null pointer, negative or too large dimension */
+    GEMM_ERR_ALIGNMENT = 2,          /* pointer not 16-byte aligned, or K % 8 or N % 8 != 0 */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 3, /* no CUDA device, or not compute capability 10.3 */
+    GEMM_ERR_OUT_OF_MEMORY = 4,      /* library-owned workspace could not be allocated */
+    GEMM_ERR_LAUNCH = 5,             /* the kernel launch failed */
+    GEMM_ERR_TIMEOUT = 6,            /* a device-side wait exceeded its limit (reported later) */
+    GEMM_ERR_CUDA = 7                /* another CUDA runtime error */
+} gemm_status_t;
+
+/* Largest accepted M, N or K (TMA coordinates are signed 32-bit). */
+#define GEMM_RELU_MAX_DIM 2147483647LL
+
+/*
+ * C = ReLU(A . B) if apply_relu != 0, else C = A . B (same rounding).
+ *
+ * A, B, C: device pointers to dense row-major binary16 matrices with leading
+ *          dimensions K, N and N.  Each must be 16-byte aligned.  C must not
+ *          overlap A or B (not checked).  The caller owns all three.
+ * M, N, K: 0 <= M, N, K <= GEMM_RELU_MAX_DIM; K and N must be multiples of
+ *          8 (the row pitch of A and B must be a multiple of 16 bytes for the
+ *          tensor-memory-accelerator copies).  M has no constraint.
+ *          M == 0 or N == 0: nothing is done.  K == 0: C is set to +0.
+ *
+ * Execution is asynchronous on `stream`; GEMM_OK means enqueued.  A device
+ * fault of this call (e.g. a timed-out wait) is reported by the next
+ * gemm_relu_check_device_error().  Shapes whose work is split along K use a
+ * library-owned fp32 workspace and arrival counters kept per (device,
+ * stream); they are grown on first need (which synchronizes that stream),
+ * so issue one call of the largest shape before capturing a CUDA graph.
+ * Calls on the same stream are ordered; calls on different streams use
+ * different workspaces and may overlap.
+ */
+int gemm_relu(const void* A, const void* B, void* C,
+              int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);
+
+/*
+ * Same operation on HOST buffers: copies A and B to library-owned device
+ * buffers (one cudaMemcpyAsync each), runs gemm_relu on `stream`, copies C
+ * back, and synchronizes `stream` before returning.  Pinned host memory
+ * gives the fastest copies; pageable memory also works.  Alignment rules on
+ * the host pointers are waived (the device copies are aligned); K % 8 and
+ * N % 8 still apply.  Returns the device error status of the call as well.
+ */
+int gemm_relu_host(const void* A_host, const void* B_host, void* C_host,
+                   int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error
+ * word.  Returns GEMM_ERR_TIMEOUT if a kernel of this library gave up a
+ * bounded wait since the last check (the split-K counters are then reset),
+ * GEMM_ERR_CUDA if the stream reports a CUDA error, else GEMM_OK.
+ */
+int gemm_relu_check_device_error(void* stream);
+
+/* Human-readable name of a gemm_status_t value (static storage). */
+const char* gemm_relu_status_string(int status);
+
+/* Frees every library-owned device buffer on every device.  Must not be
+ * called while work of this library is in flight. */
+void gemm_relu_shutdown(void);
+
+/* ---- Host-only planning interface (no CUDA calls; usable without a GPU) -- */
+
+typedef struct {
+    int32_t path;        /* 0 nothing to do, 1 zero fill (K == 0), 2 tiled, 3 swapped operands */
+    int32_t mma_m;       /* tcgen05 MMA M: 128 (C rows for path 2, C columns for path 3) */
+    int32_t mma_n;       /* tcgen05 MMA N: 128 or 256 (C columns) / padded M (path 3) */
+    int32_t tile_m;      /* C tile rows */
+    int32_t tile_n;      /* C tile columns */
+    int32_t tiles_m, tiles_n, num_tiles;
+    int32_t num_kb;      /* ceil(K / 64) */
+    int32_t group_m;     /* tile rasterisation: tiles_m are walked in groups of group_m */
+    int32_t grid;        /* persistent CTAs */
+    int32_t dp_tiles;    /* tiles [0, dp_tiles) are done whole, round-robin over CTAs */
+    int32_t sk_tiles;    /* tiles [dp_tiles, num_tiles) are split along K (stream-K) */
+    int32_t sk_q, sk_r;  /* stream-K k-blocks per CTA: q, plus 1 for CTAs < r */
+    int32_t max_slots;   /* most CTAs sharing one stream-K tile */
+    int32_t num_stages;  /* shared-memory ring depth */
+    int32_t stage_bytes; /* bytes of A and B tile per ring stage */
+    int32_t smem_bytes;  /* dynamic shared memory per CTA */
+    int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
+    int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
+    int64_t counter_count;   /* arrival counters (one per stream-K tile) */
+} gemm_relu_plan_t;
+
+/*
+ * Fills *plan with the decomposition gemm_relu uses for an M x N x K
+ * problem on a device with `num_sms` multiprocessors.  Pure host code.
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
+ */
+int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);
+
+/*
+ * The idx-th work item of CTA `cta` under *plan, exactly as the kernel walks
+ * it: C tile `tile` (tile_m_idx, tile_n_idx after rasterisation), k-blocks
+ * [kb_begin, kb_end), and for a tile split along K its share `slot` of
+ * `nslots`.  Returns 1 if the item exists, 0 past the CTA's last item,
+ * negative on bad arguments.  Pure host code (used to test the schedule).
+ */
+int gemm_relu_plan_work_item(const gemm_relu_plan_t* plan, int cta, int idx,
+                             int32_t* tile, int32_t* tile_m_idx, int32_t* tile_n_idx,
+                             int32_t* kb_begin, int32_t* kb_end,
+                             int32_t* slot, int32_t* nslots);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_RELU_H */

@@ -18,3 +18,11 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def gemm_lib():
+    """The CUDA library, built in-tree if stale (nvcc cross-compiles on CPU)."""
+    from tiled_dense_gemm_gb300 import binding, build
+    build.build()
+    return binding

@@ -1,0 +1,255 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Every comparison is elementwise |c - ref| <= 1e-2 + 1e-2 |ref| (the GEMM+ReLU
+listing's assert_close tolerance, oracle as the expected value), except the
+integer cases, which must match bit for bit.  Problems the oracle cannot
+finish in seconds are checked on whole tile-row and tile-column blocks
+(including every ragged edge) plus random rows and columns, each computed
+by the oracle exactly as it computes the full product.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_dense_gemm_gb300 import binding
+from tiled_dense_gemm_gb300.workloads import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+THREADS = max(1, len(os.sched_getaffinity(0)))
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tiled_dense_gemm_gb300 import build
+    build.build()
+    oracle.build()
+    torch.cuda.set_device(DEV)
+    yield
+    torch.cuda.synchronize()
+
+
+def gpu_run(A, B, relu=True, stream=None):
+    a, b = A.to(DEV), B.to(DEV)
+    c = binding.gemm_relu(a, b, apply_relu=relu, stream=stream)
+    binding.check_device_error(stream)
+    return c.cpu()
+
+
+def assert_close(c16, ref, what=""):
+    c = c16.double().numpy() if hasattr(c16, "double") else np.asarray(c16, np.float64)
+    assert np.isfinite(c).all(), f"{what}: non-finite outputs"
+    assert np.abs(ref).max(initial=0.0) < oracle.FP16_MAX, f"{what}: invalid workload (fp16 overflow)"
+    ok = oracle.within_tolerance(c, ref)
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i, j = bad[0]
+        err = np.abs(c - ref)
+        raise AssertionError(f"{what}: {len(bad)} of {ok.size} outside tolerance; first at "
+                             f"({i},{j}) gpu={c[i, j]!r} ref={ref[i, j]!r}; max abs err {err.max():.3g}")
+
+
+def assert_relu_sign(c16, relu):
+    if relu:
+        bits = c16.contiguous().view(torch.int16)
+        assert (bits >= 0).all(), "ReLU output has a sign bit set (negative or -0)"
+
+
+def sampled_blocks(M, N, tile_m, tile_n, seed):
+    rng = np.random.default_rng(seed)
+    rows = sorted(set(range(min(tile_m, M))) | set(range(max(0, M - tile_m - (M % tile_m)), M))
+                  | set(rng.integers(0, M, 48).tolist()))
+    cols = sorted(set(range(min(tile_n, N))) | set(range(max(0, N - tile_n - (N % tile_n)), N))
+                  | set(rng.integers(0, N, 48).tolist()))
+    return np.array(rows), np.array(cols)
+
+
+def check_sampled(A, B, C, relu, seed, what, tile_m=128, tile_n=256):
+    M, N = C.shape
+    rows, cols = sampled_blocks(M, N, tile_m, tile_n, seed)
+    ref_r = oracle.gemm_relu(A[rows], B, relu, threads=THREADS)
+    assert_close(C[rows], ref_r, what + " rows")
+    ref_c = oracle.gemm_relu(A, B[:, cols].contiguous(), relu, threads=THREADS)
+    assert_close(C[:, cols], ref_c, what + " cols")
+
+
+# ---------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("name", ["c1_256", "c2_1024", "c4_skinny"])
+def test_workload_full_parity(name):
+    w = WORKLOADS[name]
+    A, B = workload_inputs(w)
+    for relu in w.relu_modes:
+        C = gpu_run(A, B, relu)
+        ref = oracle.gemm_relu(A, B, relu, threads=THREADS)
+        assert_close(C, ref, f"{name} relu={relu}")
+        assert_relu_sign(C, relu)
+
+
+def test_square_4096_sampled_parity():
+    w = WORKLOADS["c3_4096"]
+    A, B = workload_inputs(w)
+    C = gpu_run(A, B, True)
+    check_sampled(A, B, C, True, 2, "c3_4096")
+    assert_relu_sign(C, True)
+
+
+@pytest.mark.parametrize("relu", [True, False])
+def test_ragged_sampled_parity(relu):
+    w = WORKLOADS["c5_ragged"]
+    A, B = workload_inputs(w)
+    C = gpu_run(A, B, relu)
+    check_sampled(A, B, C, relu, 4, f"c5_ragged relu={relu}")
+    assert_relu_sign(C, relu)
+
+
+def test_ragged_tail_block_full():
+    """The whole last tile row and tile column of the ragged workload."""
+    w = WORKLOADS["c5_ragged"]
+    A, B = workload_inputs(w)
+    C = gpu_run(A, B, True)
+    r0 = (w.M // 128) * 128
+    ref = oracle.gemm_relu(A[r0:], B, True, threads=THREADS)
+    assert_close(C[r0:], ref, "last tile row")
+    c0 = (w.N // 256) * 256
+    ref = oracle.gemm_relu(A, B[:, c0:].contiguous(), True, threads=THREADS)
+    assert_close(C[:, c0:], ref, "last tile column")
+
+
+# ---------------------------------------------------------------- exactness
+
+@pytest.mark.parametrize("shape", [(300, 264, 512), (16, 8192, 512), (128, 1024, 4096 // 8),
+                                   (1024, 1024, 512), (129, 136, 136)])
+def test_integer_inputs_bit_exact(shape):
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, seed=99, dist_a="intgrid", scale_a=2, dist_b="intgrid", scale_b=2)
+    for relu in (True, False):
+        C = gpu_run(A, B, relu)
+        ref = oracle.gemm_relu(A, B, relu, threads=THREADS)
+        assert np.array_equal(C.double().numpy(), ref), f"{shape} relu={relu} not bit-exact"
+
+
+def test_identity_B_gives_relu_A():
+    A, _ = make_inputs(200, 8, 256, seed=5)
+    I = torch.eye(256, dtype=torch.float16)
+    C = gpu_run(A, I, True)
+    assert torch.equal(C, torch.where(A > 0, A, torch.zeros_like(A)))
+
+
+# ---------------------------------------------------------------- edges
+
+EDGE_M = [1, 8, 127, 128, 129, 255, 257, 300]
+EDGE_N = [8, 120, 128, 136, 256, 264]
+EDGE_K = [8, 64, 72, 2056]
+NAN16 = 0x7E00
+CANARY = 0x5A5A
+GUARD = 64
+
+
+@pytest.mark.parametrize("K", EDGE_K)
+@pytest.mark.parametrize("M", EDGE_M)
+def test_edge_shapes_guarded(M, K):
+    for N in EDGE_N:
+        A, B = make_inputs(M, N, K, seed=M * 7919 + N * 31 + K, dist_a="uniform", dist_b="uniform")
+        total = GUARD + M * N + GUARD
+        buf = torch.full((total,), CANARY, dtype=torch.int16, device=DEV)
+        buf[GUARD:GUARD + M * N] = NAN16
+        c = buf[GUARD:GUARD + M * N].view(torch.float16).view(M, N)
+        binding.gemm_relu(A.to(DEV), B.to(DEV), c, apply_relu=True)
+        binding.check_device_error()
+        host = buf.cpu()
+        assert (host[:GUARD] == CANARY).all() and (host[GUARD + M * N:] == CANARY).all(), \
+            f"write outside C for {M}x{N}x{K}"
+        C = c.cpu()
+        assert not torch.isnan(C).any(), f"unwritten outputs for {M}x{N}x{K}"
+        ref = oracle.gemm_relu(A, B, True, threads=THREADS)
+        assert_close(C, ref, f"{M}x{N}x{K}")
+        assert_relu_sign(C, True)
+
+
+@pytest.mark.parametrize("shape", [(128, 128, 65536), (16, 65536, 512), (20000, 8, 8),
+                                   (130, 24, 4104), (64, 4096, 16384)])
+def test_extreme_aspect_ratios(shape):
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, seed=sum(shape), scale_a=1.0, scale_b=K ** -0.5)
+    C = gpu_run(A, B, True)
+    if M * N * K <= 2 ** 31:
+        assert_close(C, oracle.gemm_relu(A, B, True, threads=THREADS), str(shape))
+    else:
+        check_sampled(A, B, C, True, 1, str(shape))
+
+
+def test_k_zero_writes_positive_zero():
+    c = torch.full((37, 40), float("nan"), dtype=torch.float16, device=DEV)
+    a = torch.empty((37, 0), dtype=torch.float16, device=DEV)
+    b = torch.empty((0, 40), dtype=torch.float16, device=DEV)
+    binding.gemm_relu(a, b, c)
+    binding.check_device_error()
+    assert (c.cpu().view(torch.int16) == 0).all()
+
+
+def test_empty_output_is_a_noop():
+    c = torch.full((0, 16), 1.0, dtype=torch.float16, device=DEV)
+    binding.gemm_relu(torch.empty((0, 8), dtype=torch.float16, device=DEV),
+                      torch.ones((8, 16), dtype=torch.float16, device=DEV), c)
+    binding.check_device_error()
+
+
+def test_misaligned_pointer_is_rejected():
+    base = torch.zeros(64 * 64 + 1, dtype=torch.float16, device=DEV)
+    a = base[1:].view(64, 64)
+    b = torch.zeros(64, 64, dtype=torch.float16, device=DEV)
+    with pytest.raises(binding.GemmReluError) as e:
+        binding.gemm_relu(a, b)
+    assert e.value.status == 2
+
+
+# ---------------------------------------------------------------- behaviour
+
+@pytest.mark.parametrize("name", ["c4_skinny", "c5_ragged", "c2_1024"])
+def test_deterministic(name):
+    A, B = workload_inputs(name)
+    a, b = A.to(DEV), B.to(DEV)
+    c1 = binding.gemm_relu(a, b)
+    c2 = binding.gemm_relu(a, b)
+    binding.check_device_error()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_side_stream_and_back_to_back_calls():
+    A, B = workload_inputs("c2_1024")
+    a, b = A.to(DEV), B.to(DEV)
+    s = torch.cuda.Stream(DEV)
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            outs.append(binding.gemm_relu(a, b, stream=s))
+    s.synchronize()
+    binding.check_device_error(s)
+    ref = oracle.gemm_relu(A, B, True, threads=THREADS)
+    for c in outs:
+        assert_close(c.cpu(), ref, "side stream")
+
+
+def test_host_buffer_entry_point():
+    A, B = workload_inputs("c4_skinny")
+    C = binding.gemm_relu_host(A.pin_memory(), B.pin_memory())
+    assert_close(C, oracle.gemm_relu(A, B, True, threads=THREADS), "host entry point")
+    A2, B2 = workload_inputs("c1_256")
+    C2 = binding.gemm_relu_host(A2, B2, apply_relu=False)  # pageable memory too
+    assert_close(C2, oracle.gemm_relu(A2, B2, False, threads=THREADS), "host entry point pageable")
+
+
+def test_stream_k_counters_are_left_zero():
+    """Split tiles reset their arrival counters, so repeated calls stay correct."""
+    A, B = workload_inputs("c4_skinny")
+    a, b = A.to(DEV), B.to(DEV)
+    ref = oracle.gemm_relu(A, B, True, threads=THREADS)
+    for _ in range(5):
+        c = binding.gemm_relu(a, b)
+    binding.check_device_error()
+    assert_close(c.cpu(), ref, "after repeats")

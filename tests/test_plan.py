@@ -1,0 +1,118 @@
+"""Host-side schedule of the persistent kernel (CPU only, no CUDA calls).
+
+The kernel's three roles walk the work list that gemm_relu_plan_work_item
+reports, so checking it here checks what the GPU will do: every
+(tile, k-block) unit is covered exactly once, split tiles are shared by
+consecutive slots in K order, rasterisation is a bijection, and resource
+use stays inside GB300 limits.
+"""
+import random
+from collections import defaultdict
+
+import pytest
+
+from tiled_dense_gemm_gb300.workloads import WORKLOADS
+
+SMEM_LIMIT = 227 * 1024
+SHAPES = [(w.M, w.N, w.K) for w in WORKLOADS.values()] + [
+    (1, 8, 8), (8, 8, 8), (127, 8, 64), (129, 136, 72), (257, 264, 2056), (128, 128, 128),
+    (256, 512, 64), (4096, 8192, 64), (64, 4096, 16384), (1000, 1000, 8), (2048, 2048, 2048),
+    (8192, 8192, 8192), (130, 24, 4104), (16, 65536, 512), (100000, 8, 8),
+]
+
+
+def _check(gemm_lib, M, N, K, sms):
+    p = gemm_lib.plan(M, N, K, sms)
+    d = p.as_dict()
+    assert d["path"] == (3 if M <= 128 else 2)
+    assert d["mma_m"] == 128
+    if d["path"] == 3:
+        assert d["mma_n"] == ((M + 15) // 16) * 16 and d["tile_n"] == 128
+    else:
+        assert d["mma_n"] in (128, 256) and d["tile_m"] == 128
+    assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
+    assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
+    assert d["num_kb"] == (K + 63) // 64
+    assert 2 <= d["num_stages"] <= 16
+    assert d["smem_bytes"] <= SMEM_LIMIT
+    assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
+    assert 1 <= d["grid"] <= sms
+    assert d["dp_tiles"] + d["sk_tiles"] == d["num_tiles"]
+    assert d["workspace_bytes"] == d["sk_tiles"] * d["max_slots"] * 128 * d["mma_n"] * 4
+
+    cover = defaultdict(int)
+    slots = defaultdict(dict)
+    coords = {}
+    sk_units = []
+    for cta in range(d["grid"]):
+        items = gemm_lib.plan_work_items(p, cta)
+        units = 0
+        for it in items:
+            assert 0 <= it["kb0"] < it["kb1"] <= d["num_kb"]
+            assert 0 <= it["tm"] < d["tiles_m"] and 0 <= it["tn"] < d["tiles_n"]
+            if it["tile"] in coords:
+                assert coords[it["tile"]] == (it["tm"], it["tn"])
+            coords[it["tile"]] = (it["tm"], it["tn"])
+            for kb in range(it["kb0"], it["kb1"]):
+                cover[(it["tile"], kb)] += 1
+            if it["tile"] < d["dp_tiles"]:
+                assert (it["kb0"], it["kb1"], it["nslots"]) == (0, d["num_kb"], 1)
+            else:
+                units += it["kb1"] - it["kb0"]
+                assert 0 <= it["slot"] < it["nslots"] <= d["max_slots"]
+                assert it["slot"] not in slots[it["tile"]]
+                slots[it["tile"]][it["slot"]] = (it["kb0"], it["kb1"], it["nslots"])
+        if d["sk_tiles"]:
+            sk_units.append(units)
+    # every unit exactly once
+    assert len(cover) == d["num_tiles"] * d["num_kb"]
+    assert set(cover.values()) == {1}
+    # rasterisation is a bijection
+    assert len(coords) == d["num_tiles"]
+    assert len(set(coords.values())) == d["num_tiles"]
+    # split tiles: slots 0..n-1, contiguous K ranges in slot order
+    for t, s in slots.items():
+        n = next(iter(s.values()))[2]
+        assert sorted(s) == list(range(n))
+        kb = 0
+        for i in range(n):
+            assert s[i][0] == kb and s[i][2] == n
+            kb = s[i][1]
+        assert kb == d["num_kb"]
+    # stream-K runs differ by at most one k-block
+    if sk_units:
+        assert max(sk_units) - min(sk_units) <= 1
+        assert sum(sk_units) == d["sk_tiles"] * d["num_kb"]
+    return d
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("sms", [152, 148, 7])
+def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
+    _check(gemm_lib, *shape, sms)
+
+
+def test_random_shapes(gemm_lib):
+    rng = random.Random(0)
+    for _ in range(60):
+        M = rng.randint(1, 3000)
+        N = 8 * rng.randint(1, 700)
+        K = 8 * rng.randint(1, 600)
+        _check(gemm_lib, M, N, K, rng.choice([152, 148, 100, 33]))
+
+
+def test_degenerate_plans(gemm_lib):
+    assert gemm_lib.plan(0, 8, 8, 152).path == 0
+    assert gemm_lib.plan(8, 0, 8, 152).path == 0
+    assert gemm_lib.plan(8, 8, 0, 152).path == 1
+    with pytest.raises(gemm_lib.GemmReluError):
+        gemm_lib.plan(-1, 8, 8, 152)
+    with pytest.raises(gemm_lib.GemmReluError):
+        gemm_lib.plan(8, 8, 8, 0)
+
+
+def test_headline_shapes_use_the_intended_kernels(gemm_lib):
+    sq = gemm_lib.plan(4096, 4096, 4096, 152)
+    assert sq.path == 2 and sq.grid == 152
+    sk = gemm_lib.plan(16, 8192, 8192, 152)
+    assert sk.path == 3 and sk.mma_n == 16 and sk.grid == 152 and sk.sk_tiles == sk.num_tiles

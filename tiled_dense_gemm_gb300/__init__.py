@@ -5,12 +5,14 @@ The compute path is a hand-written sm_103a CUDA library behind a C ABI
 library is loaded lazily on first use so that importing this package (for
 example to draw the seeded workloads in ``workloads``) needs no GPU.
 """
+import importlib
 
-__all__ = ["gemm_relu", "workloads"]
+__all__ = ["gemm_relu", "gemm_relu_host", "binding", "workloads"]
 
 
 def __getattr__(name):
-    if name in ("gemm_relu", "gemm_relu_host", "binding"):
-        from . import binding
-        return binding if name == "binding" else getattr(binding, name)
+    if name in ("binding", "build", "workloads"):
+        return importlib.import_module(f".{name}", __name__)
+    if name in ("gemm_relu", "gemm_relu_host", "check_device_error"):
+        return getattr(importlib.import_module(".binding", __name__), name)
     raise AttributeError(name)

@@ -1,0 +1,188 @@
+"""ctypes binding to libgemmrelu.so (argument marshalling only).
+
+Every step of the computation runs in the CUDA library; this module checks
+tensor properties, passes raw pointers, sizes and the current CUDA stream,
+and turns status codes into exceptions.  There is no CPU fallback: if the
+library is missing or the device is not a GB300 (sm_103a), calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from .build import INCLUDE, LIB_PATH
+
+GEMM_OK = 0
+STATUS_NAMES = {
+    0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_ALIGNMENT",
+    3: "GEMM_ERR_UNSUPPORTED_DEVICE", 4: "GEMM_ERR_OUT_OF_MEMORY", 5: "GEMM_ERR_LAUNCH",
+    6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_CUDA",
+}
+
+
+class GemmReluError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}" if what else
+                         STATUS_NAMES.get(status, str(status)))
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "path", "mma_m", "mma_n", "tile_m", "tile_n", "tiles_m", "tiles_n", "num_tiles",
+        "num_kb", "group_m", "grid", "dp_tiles", "sk_tiles", "sk_q", "sk_r", "max_slots",
+        "num_stages", "stage_bytes", "smem_bytes", "tmem_cols")] + [
+        ("workspace_bytes", ctypes.c_int64), ("counter_count", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/gemm_relu.h declares."""
+    text = open(os.path.join(INCLUDE, "gemm_relu.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_relu\w*)\s*\(", text)))
+
+
+def lib():
+    """Load libgemmrelu.so (built by ``__graft_entry__.build()`` or
+    ``python -m tiled_dense_gemm_gb300.build``).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; build it first "
+                               "(python -m tiled_dense_gemm_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        L.gemm_relu.restype = i32
+        L.gemm_relu.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_host.restype = i32
+        L.gemm_relu_host.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_check_device_error.restype = i32
+        L.gemm_relu_check_device_error.argtypes = [vp]
+        L.gemm_relu_status_string.restype = ctypes.c_char_p
+        L.gemm_relu_status_string.argtypes = [i32]
+        L.gemm_relu_shutdown.restype = None
+        L.gemm_relu_shutdown.argtypes = []
+        L.gemm_relu_plan.restype = i32
+        L.gemm_relu_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(Plan)]
+        p32 = ctypes.POINTER(ctypes.c_int32)
+        L.gemm_relu_plan_work_item.restype = i32
+        L.gemm_relu_plan_work_item.argtypes = [ctypes.POINTER(Plan), i32, i32] + [p32] * 7
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_relu_status_string(int(status)).decode()
+
+
+def plan(M: int, N: int, K: int, num_sms: int) -> Plan:
+    p = Plan()
+    rc = lib().gemm_relu_plan(M, N, K, num_sms, ctypes.byref(p))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu_plan")
+    return p
+
+
+def plan_work_items(p: Plan, cta: int) -> list[dict]:
+    """Work items of one CTA, as the kernel walks them."""
+    out = []
+    vals = [ctypes.c_int32() for _ in range(7)]
+    idx = 0
+    while True:
+        rc = lib().gemm_relu_plan_work_item(ctypes.byref(p), cta, idx,
+                                            *[ctypes.byref(v) for v in vals])
+        if rc < 0:
+            raise GemmReluError(GEMM_OK + 1, "gemm_relu_plan_work_item")
+        if rc == 0:
+            return out
+        out.append(dict(zip(("tile", "tm", "tn", "kb0", "kb1", "slot", "nslots"),
+                            (v.value for v in vals))))
+        idx += 1
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def gemm_relu(a, b, c=None, apply_relu: bool = True, stream=None):
+    """C = ReLU(a @ b) (or a @ b) for CUDA fp16 tensors a (M, K), b (K, N).
+
+    ``c`` (M, N) fp16 is written in place when given, else allocated.  Runs
+    asynchronously on ``stream`` (default: torch's current stream)."""
+    import torch
+    if not (isinstance(a, torch.Tensor) and isinstance(b, torch.Tensor)):
+        raise TypeError("a and b must be torch tensors")
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise TypeError("a and b must be float16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"bad shapes {tuple(a.shape)} @ {tuple(b.shape)}")
+    if not (a.is_cuda and b.is_cuda) or a.device != b.device:
+        raise ValueError("a and b must be CUDA tensors on the same device")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous row-major (call .contiguous())")
+    M, K = a.shape
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float16, device=a.device)
+    elif (c.dtype != torch.float16 or tuple(c.shape) != (M, N) or c.device != a.device
+          or not c.is_contiguous()):
+        raise ValueError("c must be a contiguous float16 (M, N) tensor on a's device")
+    with torch.cuda.device(a.device):
+        rc = lib().gemm_relu(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                             int(bool(apply_relu)), _stream_handle(stream, a.device))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu")
+    return c
+
+
+def gemm_relu_host(a, b, c=None, apply_relu: bool = True, stream=None, device=None):
+    """Same operation on CPU fp16 tensors (pinned memory is fastest): the
+    library copies them to the GPU, computes, and copies C back before
+    returning."""
+    import torch
+    if a.dtype != torch.float16 or b.dtype != torch.float16 or a.is_cuda or b.is_cuda:
+        raise TypeError("a and b must be CPU float16 tensors")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"bad shapes {tuple(a.shape)} @ {tuple(b.shape)}")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous")
+    M, K = a.shape
+    N = b.shape[1]
+    if c is None:
+        c = torch.empty((M, N), dtype=torch.float16, pin_memory=a.is_pinned())
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = lib().gemm_relu_host(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                                  int(bool(apply_relu)), _stream_handle(stream, dev))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu_host")
+    return c
+
+
+def check_device_error(stream=None, device=None):
+    """Synchronize ``stream`` and raise if a kernel of this library reported
+    a timed-out wait since the last check."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = lib().gemm_relu_check_device_error(_stream_handle(stream, dev))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "device")
+
+
+def shutdown():
+    lib().gemm_relu_shutdown()

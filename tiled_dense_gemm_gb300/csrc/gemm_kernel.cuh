@@ -1,0 +1,397 @@
+// Persistent, warp-specialised C = ReLU(A . B) kernel for sm_103a.
+//
+// Per CTA (192 threads, one CTA per SM):
+//   warp 0      TMA producer: one thread streams A and B k-blocks into a
+//               ring of shared-memory stages (128-byte swizzle), each stage
+//               guarded by a full/empty mbarrier pair;
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
+//               (fp16 x fp16 -> fp32, 128 x N x 16 per instruction) into one
+//               of two TMEM accumulators and commits stage releases;
+//   warps 2-5   epilogue: TMEM -> registers (each warp owns a 32-lane
+//               quarter of the accumulator), ReLU, round to fp16, store to
+//               C; or, for a tile split along K, store an fp32 partial and
+//               let the last CTA to finish sum the partials in slot order.
+// The two accumulators let the epilogue of tile i overlap the mainloop of
+// tile i+1.  Every wait is bounded: on timeout the CTA records an error
+// word, tells its other roles to stop, lets in-flight copies and MMAs land,
+// frees its tensor memory and returns.
+//
+// The schedule follows the tile/pipeline recipe of the TileLang GEMM+ReLU
+// example ("Writing High-Performance Kernels in TileLang", GEMM section:
+// shared-memory A/B tiles, a pipelined K loop, a tile-level MMA into a
+// float accumulator, ReLU on the accumulator, copy out), rebuilt for
+// Blackwell: TMA + mbarriers instead of cp.async, tcgen05 + TMEM instead of
+// register fragments, and a persistent stream-K grid instead of one CTA per
+// tile.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace gr {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kEpiThreads = 128;
+constexpr uint32_t kEpiBarrier = 1;  // named barrier id for the epilogue warps
+constexpr int kMaxStagesDev = 16;
+constexpr uint32_t kOperandA = 128 * kBlockK * 2;  // bytes of the MMA A operand per stage
+constexpr uint32_t kSwizzleRow = 128;              // bytes per swizzled row
+constexpr uint32_t kAtomBytes = 1024;              // 8 swizzled rows
+constexpr uint32_t kChunkBytes = kBlockK * kSwizzleRow;  // one 64-wide M/N chunk of 64 k-rows
+
+enum : int32_t {
+    kErrProducer = 0x11,
+    kErrMmaStage = 0x21,
+    kErrMmaAccum = 0x22,
+    kErrEpilogue = 0x31,
+    kErrFinal = 0x41,
+};
+
+struct __align__(8) Ctrl {
+    uint64_t full[kMaxStagesDev];
+    uint64_t empty[kMaxStagesDev];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t final_bar;
+    uint32_t tmem_addr;
+    int32_t abort_flag;
+    int32_t last_flag;
+};
+static_assert(sizeof(Ctrl) <= 1024, "control block exceeds its reserved 1 KiB");
+
+struct KParams {
+    gemm_relu_plan_t plan;
+    int64_t M, N, K;
+    int32_t apply_relu;
+    uint32_t idesc;
+    uint64_t timeout_ns;
+    __half* C;
+    float* ws;            // stream-K partial tiles: [sk_tile][slot][col][128 lanes]
+    uint32_t* counters;   // stream-K arrivals, one per stream-K tile, zero between launches
+    int32_t* err;         // first error code of the launch (0 = none)
+};
+
+// kMode 0: C tile 128 x 256; 1: C tile 128 x 128; 2: swapped operands
+// (C tile mpad x 128: B^T is the MMA A operand, A^T the MMA B operand).
+template <int kMode>
+struct ModeTraits {
+    static constexpr bool kSwap = (kMode == 2);
+    static constexpr uint32_t kBN = (kMode == 0) ? 256 : 128;  // C columns per tile (normal)
+    static constexpr int kCols = kSwap ? 16 : 32;              // TMEM columns per epilogue load
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Ctrl* ctrl,
+                                           const KParams& p, int32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    volatile int32_t* abort_flag = &ctrl->abort_flag;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            *abort_flag = 1;
+            atomicCAS(p.err, 0, site);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used at teardown, when the
+// point is to let outstanding work finish).
+__device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
+__device__ __forceinline__ float relu_if(float x, int32_t apply) {
+    // x > 0 ? x : +0 also maps -0 and NaN to +0
+    return apply ? (x > 0.0f ? x : 0.0f) : x;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int kMode>
+__device__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
+                              const CUtensorMap* tmA, const CUtensorMap* tmB) {
+    using T = ModeTraits<kMode>;
+    const gemm_relu_plan_t& pl = p.plan;
+    const uint32_t S = (uint32_t)pl.num_stages;
+    WorkIter wi;
+    wi.init(pl, blockIdx.x);
+    WorkItem w;
+    uint32_t it = 0;
+    while (wi.next(pl, w)) {
+        for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            const uint32_t s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!wait_phase(smem_u32(&ctrl->empty[s]), ph ^ 1u, ctrl, p, kErrProducer)) return;
+            const uint32_t full = smem_u32(&ctrl->full[s]);
+            const uint32_t a_dst = stages + s * stride;
+            const uint32_t b_dst = a_dst + kOperandA;
+            const int32_t k0 = kb * kBlockK;
+            mbar_arrive_expect_tx(full, (uint32_t)pl.stage_bytes);
+            if constexpr (!T::kSwap) {
+                tma_load_2d(a_dst, tmA, full, k0, w.tm * 128);
+#pragma unroll
+                for (uint32_t j = 0; j < T::kBN / 64; ++j)
+                    tma_load_2d(b_dst + j * kChunkBytes, tmB, full, w.tn * (int32_t)T::kBN + 64 * j, k0);
+            } else {
+                tma_load_2d(a_dst, tmB, full, w.tn * 128, k0);
+                tma_load_2d(a_dst + kChunkBytes, tmB, full, w.tn * 128 + 64, k0);
+                tma_load_2d(b_dst, tmA, full, k0, w.tm * pl.tile_m);
+            }
+        }
+    }
+}
+
+template <int kMode>
+__device__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
+                         uint32_t tmem_base) {
+    using T = ModeTraits<kMode>;
+    const gemm_relu_plan_t& pl = p.plan;
+    const uint32_t S = (uint32_t)pl.num_stages;
+    const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
+    WorkIter wi;
+    wi.init(pl, blockIdx.x);
+    WorkItem w;
+    uint32_t it = 0, local = 0;
+    while (wi.next(pl, w)) {
+        const uint32_t buf = local & 1u;
+        const uint32_t bph = (local >> 1) & 1u;
+        if (!wait_phase(smem_u32(&ctrl->tmem_empty[buf]), bph ^ 1u, ctrl, p, kErrMmaAccum)) return;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * cols_per_buf;
+        for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            const uint32_t s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!wait_phase(smem_u32(&ctrl->full[s]), ph, ctrl, p, kErrMmaStage)) return;
+            tc_fence_after();
+            const uint32_t a_base = stages + s * stride;
+            const uint32_t b_base = a_base + kOperandA;
+#pragma unroll
+            for (uint32_t k = 0; k < kBlockK / 16; ++k) {
+                uint64_t adesc, bdesc;
+                if constexpr (!T::kSwap) {
+                    // A: K-major, advance 16 k = 32 bytes inside the swizzled row
+                    adesc = make_sw128_desc(a_base + k * 32, 16, kAtomBytes);
+                    // B: N-major, advance 16 k-rows = 2 atoms
+                    bdesc = make_sw128_desc(b_base + k * 2 * kAtomBytes, kChunkBytes, kAtomBytes);
+                } else {
+                    adesc = make_sw128_desc(a_base + k * 2 * kAtomBytes, kChunkBytes, kAtomBytes);
+                    bdesc = make_sw128_desc(b_base + k * 32, 16, kAtomBytes);
+                }
+                mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&ctrl->empty[s]));  // stage free once these MMAs are done
+        }
+        mma_commit(smem_u32(&ctrl->tmem_full[buf]));  // accumulator ready
+        ++local;
+    }
+}
+
+// Store one epilogue chunk (kCols accumulator columns of this thread's
+// TMEM lane) to C.
+template <int kMode>
+__device__ __forceinline__ void store_chunk(const KParams& p, const WorkItem& w, uint32_t lane_row,
+                                            uint32_t col0, const float* v) {
+    using T = ModeTraits<kMode>;
+    if constexpr (!T::kSwap) {
+        const int64_t m = (int64_t)w.tm * 128 + lane_row;
+        if (m >= p.M) return;
+        const int64_t n0 = (int64_t)w.tn * T::kBN + col0;
+        __half* dst = p.C + m * p.N + n0;
+#pragma unroll
+        for (int g = 0; g < T::kCols / 8; ++g) {
+            if (n0 + 8 * g < p.N) {  // N % 8 == 0: an 8-column group is all in or all out
+                uint4 q;
+                q.x = pack_half2(relu_if(v[8 * g + 0], p.apply_relu), relu_if(v[8 * g + 1], p.apply_relu));
+                q.y = pack_half2(relu_if(v[8 * g + 2], p.apply_relu), relu_if(v[8 * g + 3], p.apply_relu));
+                q.z = pack_half2(relu_if(v[8 * g + 4], p.apply_relu), relu_if(v[8 * g + 5], p.apply_relu));
+                q.w = pack_half2(relu_if(v[8 * g + 6], p.apply_relu), relu_if(v[8 * g + 7], p.apply_relu));
+                *reinterpret_cast<uint4*>(dst + 8 * g) = q;
+            }
+        }
+    } else {
+        const int64_t n = (int64_t)w.tn * 128 + lane_row;
+        if (n >= p.N) return;
+        const int64_t m0 = (int64_t)w.tm * p.plan.tile_m + col0;
+#pragma unroll
+        for (int j = 0; j < T::kCols; ++j) {
+            const int64_t m = m0 + j;
+            if (m < p.M) p.C[m * p.N + n] = __float2half_rn(relu_if(v[j], p.apply_relu));
+        }
+    }
+}
+
+template <int kMode>
+__device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
+    using T = ModeTraits<kMode>;
+    if constexpr (T::kCols == 32) {
+        tmem_load_32cols(taddr, *reinterpret_cast<float(*)[32]>(v));
+    } else {
+        tmem_load_16cols(taddr, *reinterpret_cast<float(*)[16]>(v));
+    }
+}
+
+template <int kMode>
+__device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base) {
+    using T = ModeTraits<kMode>;
+    const gemm_relu_plan_t& pl = p.plan;
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
+    const uint32_t lane_row = quarter * 32 + lane;
+    const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
+    const uint32_t ncols = (uint32_t)pl.mma_n;
+    const int64_t tile_elems = (int64_t)128 * ncols;
+    volatile int32_t* last_flag = &ctrl->last_flag;
+    WorkIter wi;
+    wi.init(pl, blockIdx.x);
+    WorkItem w;
+    uint32_t local = 0;
+    float v[T::kCols];
+    while (wi.next(pl, w)) {
+        const uint32_t buf = local & 1u;
+        const uint32_t bph = (local >> 1) & 1u;
+        bool ok = wait_phase(smem_u32(&ctrl->tmem_full[buf]), bph, ctrl, p, kErrEpilogue);
+        ok = named_bar_and(kEpiBarrier, kEpiThreads, ok);  // all epilogue warps agree
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + buf * cols_per_buf;
+        float* part = nullptr;
+        if (w.nslots > 1)
+            part = p.ws + ((int64_t)w.sk_index * pl.max_slots + w.slot) * tile_elems;
+        for (uint32_t c = 0; c < ncols; c += T::kCols) {
+            __syncwarp();  // tcgen05.ld is warp-collective
+            tmem_load_chunk<kMode>(taddr + c, v);
+            if (w.nslots == 1) {
+                store_chunk<kMode>(p, w, lane_row, c, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < T::kCols; ++j) __stcg(part + (int64_t)(c + j) * 128 + lane_row, v[j]);
+            }
+        }
+        // accumulator buffer back to the MMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
+        if (w.nslots > 1) {
+            // publish the partial, count arrivals; the last CTA reduces
+            __threadfence();
+            named_bar_sync(kEpiBarrier, kEpiThreads);
+            if (threadIdx.x == 64) {
+                const uint32_t prev = atomicAdd(&p.counters[w.sk_index], 1u);
+                const int32_t last = (prev == (uint32_t)(w.nslots - 1)) ? 1 : 0;
+                if (last) p.counters[w.sk_index] = 0u;  // ready for the next launch
+                *last_flag = last;
+            }
+            named_bar_sync(kEpiBarrier, kEpiThreads);
+            if (*last_flag) {
+                __threadfence();
+                const float* base = p.ws + (int64_t)w.sk_index * pl.max_slots * tile_elems;
+                for (uint32_t c = 0; c < ncols; c += T::kCols) {
+#pragma unroll
+                    for (int j = 0; j < T::kCols; ++j) v[j] = 0.0f;
+                    for (int32_t s = 0; s < w.nslots; ++s) {
+                        const float* src = base + (int64_t)s * tile_elems + (int64_t)c * 128 + lane_row;
+#pragma unroll
+                        for (int j = 0; j < T::kCols; ++j) v[j] += __ldcg(src + (int64_t)j * 128);
+                    }
+                    store_chunk<kMode>(p, w, lane_row, c, v);
+                }
+            }
+        }
+        ++local;
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
+    const uint32_t base = smem_u32(smem);
+    const uint32_t stages = (base + (uint32_t)sizeof(Ctrl) + 1023u) & ~1023u;
+    const gemm_relu_plan_t& pl = p.plan;
+    const uint32_t a_bytes = kOperandA;
+    const uint32_t b_bytes = ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u;
+    const uint32_t stride = a_bytes + b_bytes;
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < pl.num_stages; ++s) {
+            mbar_init(smem_u32(&ctrl->full[s]), 1);
+            mbar_init(smem_u32(&ctrl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);
+            mbar_init(smem_u32(&ctrl->tmem_empty[b]), kEpiThreads / 32);
+        }
+        mbar_init(smem_u32(&ctrl->final_bar), 1);
+        ctrl->abort_flag = 0;
+        ctrl->last_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctrl->tmem_addr;
+
+    if (warp == 0) {
+        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, &tmA, &tmB);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            mma_role<kMode>(p, ctrl, stages, stride, tmem_base);
+            // no MMA may still be writing TMEM when it is released
+            mma_commit(smem_u32(&ctrl->final_bar));
+            if (!wait_phase_for(smem_u32(&ctrl->final_bar), 0, p.timeout_ns)) atomicCAS(p.err, 0, kErrFinal);
+        }
+        __syncwarp();
+    } else {
+        epilogue_role<kMode>(p, ctrl, tmem_base);
+    }
+
+    if (warp == 0 && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
+        // aborting: give copies already issued time to land before the
+        // shared memory is released
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 100000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, (uint32_t)pl.tmem_cols);
+    }
+}
+
+__global__ void zero_fill_kernel(uint4* c, int64_t n16) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        c[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+}  // namespace gr

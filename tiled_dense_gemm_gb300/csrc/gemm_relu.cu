@@ -1,0 +1,366 @@
+// C ABI of the GB300 gemm_relu library: argument checks, per-device state,
+// tensor-map encoding, workspace management and kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "gemm_kernel.cuh"
+#include "gemm_relu.h"
+
+namespace gr {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxDynSmem = 227 * 1024;  // sm_100-family opt-in limit per CTA
+
+struct StreamBuffers {
+    void* stream = nullptr;
+    float* ws = nullptr;  // stream-K partial tiles
+    size_t ws_bytes = 0;
+    uint32_t* counters = nullptr;  // stream-K arrival counters (kept zero between launches)
+    size_t n_counters = 0;
+    void* hA = nullptr;  // staging for the host-buffer entry point
+    void* hB = nullptr;
+    void* hC = nullptr;
+    size_t hA_bytes = 0, hB_bytes = 0, hC_bytes = 0;
+};
+
+struct DeviceState {
+    bool inited = false;
+    int status = GEMM_OK;
+    int sm_count = 0;
+    int32_t* d_err = nullptr;
+    bool attr_set[3] = {false, false, false};
+    std::vector<StreamBuffers> streams;
+};
+
+struct PlanKey {
+    int64_t M, N, K;
+    bool operator==(const PlanKey& o) const { return M == o.M && N == o.N && K == o.K; }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey& k) const {
+        uint64_t h = (uint64_t)k.M * 0x9E3779B97F4A7C15ull;
+        h ^= (uint64_t)k.N + 0x7F4A7C159E3779B9ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.K + 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        return (size_t)h;
+    }
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::unordered_map<PlanKey, gemm_relu_plan_t, PlanKeyHash> g_plans[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int init_device_locked(int dev) {
+    DeviceState& d = g_dev[dev];
+    if (d.inited) return d.status;
+    d.inited = true;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (major != 10 || minor != 3) return d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+    int optin = 0;
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (optin < kMaxDynSmem) return d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (cudaMalloc(&d.d_err, 16) != cudaSuccess) {
+        cudaGetLastError();
+        d.inited = false;
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(d.d_err, 0, 16) != cudaSuccess) {
+        cudaGetLastError();
+        return d.status = GEMM_ERR_CUDA;
+    }
+    return d.status = GEMM_OK;
+}
+
+int current_device(int* dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (*dev < 0 || *dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    return GEMM_OK;
+}
+
+StreamBuffers& buffers_for_locked(DeviceState& d, void* stream) {
+    for (auto& s : d.streams)
+        if (s.stream == stream) return s;
+    d.streams.emplace_back();
+    d.streams.back().stream = stream;
+    return d.streams.back();
+}
+
+// Grow (never shrink) one device buffer.  Synchronizes `stream` first so no
+// launch still reads the old one.
+int grow(void** buf, size_t* have, size_t need, cudaStream_t stream, bool zero) {
+    if (*have >= need) return GEMM_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (*buf) cudaFree(*buf);
+    *buf = nullptr;
+    *have = 0;
+    size_t bytes = need + need / 4;  // headroom against repeated small growth
+    if (cudaMalloc(buf, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        *buf = nullptr;
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    if (zero && cudaMemset(*buf, 0, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    *have = bytes;
+    return GEMM_OK;
+}
+
+int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};  // bytes between rows
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+}
+
+template <int kMode>
+int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, const CUtensorMap& ta,
+                const CUtensorMap& tb, cudaStream_t st) {
+    auto fn = gemm_relu_kernel<kMode>;
+    if (!d.attr_set[kMode]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        d.attr_set[kMode] = true;
+    }
+    fn<<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, kp);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return GEMM_OK;
+}
+
+int check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+               bool device_ptrs) {
+    if (M < 0 || N < 0 || K < 0 || M > GEMM_RELU_MAX_DIM || N > GEMM_RELU_MAX_DIM ||
+        K > GEMM_RELU_MAX_DIM)
+        return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_ALIGNMENT;
+    if (device_ptrs) {
+        if (((uintptr_t)C & 15u) != 0) return GEMM_ERR_ALIGNMENT;
+        if (K > 0 && ((((uintptr_t)A) | ((uintptr_t)B)) & 15u) != 0) return GEMM_ERR_ALIGNMENT;
+    }
+    return GEMM_OK;
+}
+
+int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+               int apply_relu, cudaStream_t st, int dev) {
+    DeviceState& d = g_dev[dev];
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (K == 0) {
+        const int64_t n16 = M * N * 2 / 16;  // N % 8 == 0
+        int blocks = (int)((n16 + 255) / 256);
+        const int cap = d.sm_count * 8;
+        if (blocks > cap) blocks = cap;
+        zero_fill_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<uint4*>(C), n16);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
+    }
+    gemm_relu_plan_t pl;
+    {
+        auto& cache = g_plans[dev];
+        PlanKey key{M, N, K};
+        auto itp = cache.find(key);
+        if (itp != cache.end()) {
+            pl = itp->second;
+        } else {
+            int rc = gemm_relu_plan(M, N, K, d.sm_count, &pl);
+            if (rc != GEMM_OK) return rc;
+            if (cache.size() > 4096) cache.clear();
+            cache.emplace(key, pl);
+        }
+    }
+    KParams kp;
+    memset(&kp, 0, sizeof(kp));
+    kp.plan = pl;
+    kp.M = M;
+    kp.N = N;
+    kp.K = K;
+    kp.apply_relu = apply_relu ? 1 : 0;
+    kp.C = reinterpret_cast<__half*>(C);
+    kp.err = d.d_err;
+    // generous bound: 2 s plus 2 us per k-block of the longest wait
+    kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
+    if (pl.sk_tiles > 0) {
+        StreamBuffers& sb = buffers_for_locked(d, st);
+        int rc = grow(reinterpret_cast<void**>(&sb.ws), &sb.ws_bytes, (size_t)pl.workspace_bytes, st, false);
+        if (rc != GEMM_OK) return rc;
+        rc = grow(reinterpret_cast<void**>(&sb.counters), &sb.n_counters,
+                  (size_t)pl.counter_count * sizeof(uint32_t), st, true);
+        if (rc != GEMM_OK) return rc;
+        kp.ws = sb.ws;
+        kp.counters = sb.counters;
+    }
+    CUtensorMap ta, tb;
+    const bool swap = (pl.path == 3);
+    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u);
+    if (rc != GEMM_OK) return rc;
+    rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K, 64, kBlockK);
+    if (rc != GEMM_OK) return rc;
+    if (swap) {
+        kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
+        return launch_mode<2>(d, pl, kp, ta, tb, st);
+    }
+    kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);
+    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, st);
+    return launch_mode<1>(d, pl, kp, ta, tb, st);
+}
+
+}  // namespace
+}  // namespace gr
+
+using namespace gr;
+
+extern "C" int gemm_relu(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int apply_relu, void* stream) {
+    int rc = check_args(A, B, C, M, N, K, true);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;  // nothing to enqueue
+    int dev;
+    if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if ((rc = init_device_locked(dev)) != GEMM_OK) return rc;
+    return run_device(A, B, C, M, N, K, apply_relu, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
+                              int64_t N, int64_t K, int apply_relu, void* stream) {
+    int rc = check_args(A_host, B_host, C_host, M, N, K, false);
+    if (rc != GEMM_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_OK;
+    int dev;
+    if ((rc = current_device(&dev)) != GEMM_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if ((rc = init_device_locked(dev)) != GEMM_OK) return rc;
+        DeviceState& d = g_dev[dev];
+        StreamBuffers& sb = buffers_for_locked(d, stream);
+        const size_t a_bytes = (size_t)M * K * 2, b_bytes = (size_t)K * N * 2, c_bytes = (size_t)M * N * 2;
+        if ((rc = grow(&sb.hA, &sb.hA_bytes, a_bytes > 16 ? a_bytes : 16, st, false)) != GEMM_OK) return rc;
+        if ((rc = grow(&sb.hB, &sb.hB_bytes, b_bytes > 16 ? b_bytes : 16, st, false)) != GEMM_OK) return rc;
+        if ((rc = grow(&sb.hC, &sb.hC_bytes, c_bytes, st, false)) != GEMM_OK) return rc;
+        if (a_bytes && cudaMemcpyAsync(sb.hA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        if (rc == GEMM_OK && b_bytes &&
+            cudaMemcpyAsync(sb.hB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        if (rc == GEMM_OK) rc = run_device(sb.hA, sb.hB, sb.hC, M, N, K, apply_relu, st, dev);
+        if (rc == GEMM_OK &&
+            cudaMemcpyAsync(C_host, sb.hC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
+        if (rc != GEMM_OK) {
+            cudaGetLastError();
+            return rc;
+        }
+    }
+    return gemm_relu_check_device_error(stream);
+}
+
+extern "C" int gemm_relu_check_device_error(void* stream) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc != GEMM_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.inited || !d.d_err) return d.inited ? d.status : GEMM_OK;
+    int32_t err = 0;
+    if (cudaMemcpy(&err, d.d_err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (err == 0) return GEMM_OK;
+    // a launch gave up part-way: clear the error word and every counter
+    cudaDeviceSynchronize();
+    cudaMemset(d.d_err, 0, 16);
+    for (auto& s : d.streams)
+        if (s.counters) cudaMemset(s.counters, 0, s.n_counters);
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+    return GEMM_ERR_TIMEOUT;
+}
+
+extern "C" const char* gemm_relu_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "GEMM_ERR_UNSUPPORTED_DEVICE";
+        case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+extern "C" void gemm_relu_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int prev = -1;
+    const bool have_dev = cudaGetDevice(&prev) == cudaSuccess;
+    cudaGetLastError();
+    for (int dev = 0; dev < kMaxDevices; ++dev) {
+        DeviceState& d = g_dev[dev];
+        if (!d.inited) continue;
+        if (d.d_err || !d.streams.empty()) {
+            cudaSetDevice(dev);
+            cudaDeviceSynchronize();
+            for (auto& s : d.streams) {
+                cudaFree(s.ws);
+                cudaFree(s.counters);
+                cudaFree(s.hA);
+                cudaFree(s.hB);
+                cudaFree(s.hC);
+            }
+            cudaFree(d.d_err);
+        }
+        d = DeviceState();
+        g_plans[dev].clear();
+    }
+    if (have_dev) cudaSetDevice(prev);
+    cudaGetLastError();
+}

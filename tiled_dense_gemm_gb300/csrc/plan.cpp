@@ -1,0 +1,233 @@
+// Host planner: picks tile shape, operand roles and the data-parallel /
+// stream-K split for one problem size, by a small cost model evaluated
+// over the exact work lists the kernel will walk.  Pure host code.
+#include <stdint.h>
+#include <string.h>
+
+#include "gemm_relu.h"
+#include "schedule.h"
+
+namespace gr {
+
+// Shared-memory layout constants (must match the kernel).
+constexpr int32_t kCtrlBytes = 1024;        // barriers + flags
+constexpr int32_t kAlignSlack = 1024;       // dynamic smem rounded up to 1 KiB
+constexpr int32_t kStageBudget = 200 * 1024;
+constexpr int32_t kMaxStages = 16;
+constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
+
+// Cost model, in SM clock cycles.  Rough per-k-block costs of the three
+// kernel shapes; calibrated against measurements on GB300.
+struct Costs {
+    double kb;          // one k-block through the mainloop
+    double fill;        // CTA start: barrier init, TMEM alloc, pipeline fill
+    double tile_store;  // writing one finished fp16 tile
+    double partial;     // writing one fp32 partial tile
+    double reduce_per_slot;  // reading one partial during the fixup
+};
+
+static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
+    Costs c;
+    const double tile_elems = 128.0 * mma_n;
+    if (path == 2) {
+        // 4 MMAs of 128 x N x 16 per k-block; the tensor pipe does
+        // 8192 fp16 FLOP per SM per clock.  N = 128 is also bound by
+        // shared-memory bandwidth, hence the extra factor.
+        const double mma = 4.0 * 128.0 * mma_n * 16.0 * 2.0 / 8192.0;
+        c.kb = (mma_n >= 256) ? mma : mma * 1.2;
+    } else {
+        // Swapped operands for small M: streaming B from HBM dominates.
+        // ~6.8 TB/s over 152 SMs at ~1.9 GHz is ~24 bytes per SM-clock.
+        const double mem = stage_bytes / 24.0;
+        const double mma = 4.0 * 128.0 * mma_n * 16.0 * 2.0 / 8192.0;
+        c.kb = mem > mma ? mem : mma;
+    }
+    c.fill = 2500.0;
+    c.tile_store = tile_elems * 2.0 / 64.0;
+    c.partial = tile_elems * 4.0 / 64.0;
+    c.reduce_per_slot = tile_elems * 4.0 / 64.0;
+    return c;
+}
+
+// Makespan estimate of a filled-in plan: the slowest CTA's mainloop time
+// plus its exposed epilogue work.  A finished tile's store mostly overlaps
+// the next tile's mainloop (double-buffered accumulator), so only a quarter
+// of it is counted, except for the CTA's last tile.  For a split tile the
+// slot-0 owner reaches its share last (it is the end of its run), so it is
+// charged the fixup.
+static double estimate(const gemm_relu_plan_t& p, const Costs& c) {
+    double worst = 0.0;
+    for (int32_t cta = 0; cta < p.grid; ++cta) {
+        WorkIter wi;
+        wi.init(p, cta);
+        const int32_t dp_n = wi.dp_n;
+        double t = c.fill + (double)dp_n * ((double)p.num_kb * c.kb + 0.25 * c.tile_store);
+        wi.dp_i = dp_n;  // data-parallel items are costed above
+        bool any = dp_n > 0;
+        WorkItem w;
+        while (wi.next(p, w)) {
+            any = true;
+            t += (double)(w.kb1 - w.kb0) * c.kb;
+            if (w.nslots == 1)
+                t += 0.25 * c.tile_store;
+            else
+                t += c.partial + (w.slot == 0 ? w.nslots * c.reduce_per_slot + c.tile_store : 0.0);
+        }
+        if (!any) continue;
+        t += 0.75 * c.tile_store;
+        if (t > worst) worst = t;
+    }
+    return worst;
+}
+
+static int32_t compute_max_slots(const gemm_relu_plan_t& p) {
+    int32_t best = 1;
+    for (int32_t t = 0; t < p.sk_tiles; ++t) {
+        const int32_t first = sk_owner(p, (int64_t)t * p.num_kb);
+        const int32_t last = sk_owner(p, (int64_t)(t + 1) * p.num_kb - 1);
+        if (last - first + 1 > best) best = last - first + 1;
+    }
+    return best;
+}
+
+static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t sk) {
+    p.grid = grid;
+    p.dp_tiles = dp;
+    p.sk_tiles = sk;
+    if (sk > 0) {
+        const int64_t units = (int64_t)sk * p.num_kb;
+        p.sk_q = (int32_t)(units / grid);
+        p.sk_r = (int32_t)(units % grid);
+        p.max_slots = compute_max_slots(p);
+    } else {
+        p.sk_q = p.sk_r = 0;
+        p.max_slots = 1;
+    }
+    p.workspace_bytes = (int64_t)sk * p.max_slots * p.mma_m * p.mma_n * 4;
+    p.counter_count = sk;
+}
+
+// Fill the shape-dependent fields for one kernel shape.
+static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path,
+                       int32_t mma_n) {
+    p.path = path;
+    p.mma_m = 128;
+    p.mma_n = mma_n;
+    if (path == 2) {
+        p.tile_m = 128;
+        p.tile_n = mma_n;
+    } else {
+        p.tile_m = mma_n;  // padded M
+        p.tile_n = 128;
+    }
+    p.tiles_m = (int32_t)((M + p.tile_m - 1) / p.tile_m);
+    p.tiles_n = (int32_t)((N + p.tile_n - 1) / p.tile_n);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.num_kb = (int32_t)((K + kBlockK - 1) / kBlockK);
+    p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
+    const int32_t b_bytes = mma_n * kBlockK * 2;
+    p.stage_bytes = kOperandABytes + b_bytes;
+    const int32_t stride = kOperandABytes + ((b_bytes + 1023) / 1024) * 1024;
+    int32_t stages = kStageBudget / stride;
+    if (stages > kMaxStages) stages = kMaxStages;
+    p.num_stages = stages;
+    p.smem_bytes = kCtrlBytes + kAlignSlack + stages * stride;
+    int32_t cols = 2 * mma_n;
+    int32_t alloc = 32;
+    while (alloc < cols) alloc *= 2;
+    p.tmem_cols = alloc;
+}
+
+// Choose the best split for the current shape; returns its estimated cost.
+static double choose_split(gemm_relu_plan_t& p, int32_t sms) {
+    const Costs c = costs_for(p.path, p.mma_n, p.stage_bytes);
+    const int32_t T = p.num_tiles;
+    gemm_relu_plan_t best = p;
+    double best_cost = -1.0;
+    auto consider = [&](int32_t grid, int32_t dp, int32_t sk) {
+        if (grid < 1) return;
+        if (sk > 0 && (int64_t)sk * p.num_kb < grid) grid = (int32_t)((int64_t)sk * p.num_kb);
+        gemm_relu_plan_t q = p;
+        finish_split(q, grid, dp, sk);
+        double cost = estimate(q, c);
+        // small preference for fewer partial tiles at equal cost
+        cost += 1e-3 * (double)q.sk_tiles;
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
+            best = q;
+        }
+    };
+    // plain data-parallel
+    consider(T < sms ? T : sms, T, 0);
+    if (T >= sms) {
+        const int32_t full = T / sms;
+        if (T % sms != 0) consider(sms, (full - 1) * sms, T - (full - 1) * sms);
+    } else if (p.num_kb > 1) {
+        // fewer tiles than SMs: split every tile along K over more CTAs
+        for (int32_t g = T + 1; g <= sms; ++g) consider(g, 0, T);
+    }
+    p = best;
+    return best_cost;
+}
+
+}  // namespace gr
+
+extern "C" int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms,
+                              gemm_relu_plan_t* plan) {
+    using namespace gr;
+    if (!plan || M < 0 || N < 0 || K < 0 || M > GEMM_RELU_MAX_DIM || N > GEMM_RELU_MAX_DIM ||
+        K > GEMM_RELU_MAX_DIM || num_sms < 1)
+        return GEMM_ERR_INVALID_ARG;
+    memset(plan, 0, sizeof(*plan));
+    if (M == 0 || N == 0) {
+        plan->path = 0;
+        return GEMM_OK;
+    }
+    if (K == 0) {
+        plan->path = 1;
+        return GEMM_OK;
+    }
+    // tile and k-block counts must fit 32-bit work indices
+    const int64_t kb = (K + kBlockK - 1) / kBlockK;
+    const int64_t tiles_small = ((M + 127) / 128) * ((N + 127) / 128);
+    if (tiles_small > (int64_t)1 << 30 || kb > (int64_t)1 << 30) return GEMM_ERR_INVALID_ARG;
+
+    if (M <= 128) {
+        // small M: C^T = B^T A^T, so N runs along the 128-wide MMA M side
+        // and M (padded to 16) is the MMA N side.
+        const int32_t mpad = (int32_t)((M + 15) / 16) * 16;
+        shape_plan(*plan, M, N, K, 3, mpad);
+        choose_split(*plan, num_sms);
+        return GEMM_OK;
+    }
+    gemm_relu_plan_t a, b;
+    memset(&a, 0, sizeof(a));
+    memset(&b, 0, sizeof(b));
+    shape_plan(a, M, N, K, 2, 256);
+    shape_plan(b, M, N, K, 2, 128);
+    const double ca = choose_split(a, num_sms);
+    const double cb = choose_split(b, num_sms);
+    *plan = (cb < ca) ? b : a;
+    return GEMM_OK;
+}
+
+extern "C" int gemm_relu_plan_work_item(const gemm_relu_plan_t* plan, int cta, int idx,
+                                        int32_t* tile, int32_t* tile_m_idx, int32_t* tile_n_idx,
+                                        int32_t* kb_begin, int32_t* kb_end, int32_t* slot,
+                                        int32_t* nslots) {
+    using namespace gr;
+    if (!plan || cta < 0 || idx < 0 || plan->path < 2 || cta >= plan->grid) return -1;
+    WorkIter wi;
+    wi.init(*plan, cta);
+    WorkItem w;
+    for (int i = 0; i <= idx; ++i)
+        if (!wi.next(*plan, w)) return 0;
+    if (tile) *tile = w.tile;
+    if (tile_m_idx) *tile_m_idx = w.tm;
+    if (tile_n_idx) *tile_n_idx = w.tn;
+    if (kb_begin) *kb_begin = w.kb0;
+    if (kb_end) *kb_end = w.kb1;
+    if (slot) *slot = w.slot;
+    if (nslots) *nslots = w.nslots;
+    return 1;
+}

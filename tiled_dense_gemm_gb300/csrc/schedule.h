@@ -1,0 +1,118 @@
+// Work decomposition shared by the host planner and the persistent kernel.
+//
+// The output C is cut into tiles (tile_m x tile_n).  Each tile is a
+// reduction over num_kb k-blocks of 64.  A persistent grid of `grid` CTAs
+// walks:
+//   1. data-parallel tiles [0, dp_tiles): CTA c takes tiles c, c+grid, ...,
+//      each over its whole K range;
+//   2. stream-K tiles [dp_tiles, num_tiles): their (tile, k-block) units are
+//      laid end to end and cut into `grid` contiguous runs of q or q+1 units
+//      (the first r CTAs take q+1).  A run may start or end inside a tile;
+//      the CTAs sharing a tile each own one "slot" of it, numbered in K
+//      order, and the last one to finish adds the slots' fp32 partial tiles
+//      in slot order (so the result does not depend on which CTA is last).
+// This generalises the split-KV decode idea of the TileLang MLA example
+// ("Writing High-Performance Kernels in TileLang", MLA section: spread a
+// long reduction over idle SMs and combine the pieces) to the K dimension
+// of a GEMM.
+#pragma once
+
+#include <stdint.h>
+
+#include "gemm_relu.h"
+
+#if defined(__CUDACC__)
+#define GR_HD __host__ __device__ __forceinline__
+#else
+#define GR_HD inline
+#endif
+
+namespace gr {
+
+constexpr int kBlockK = 64;  // k-block: 64 fp16 = one 128-byte swizzle row
+
+// Rasterisation: tiles are numbered so that a group of `group_m` tile rows
+// is walked column by column; CTAs running at the same time then share A
+// row-panels and B column-panels in L2.
+GR_HD void tile_coords(const gemm_relu_plan_t& p, int32_t t, int32_t& tm, int32_t& tn) {
+    const int32_t per_group = p.group_m * p.tiles_n;
+    const int32_t g = t / per_group;
+    const int32_t first_m = g * p.group_m;
+    const int32_t rows = (p.tiles_m - first_m) < p.group_m ? (p.tiles_m - first_m) : p.group_m;
+    const int32_t r = t - g * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+// First stream-K unit of CTA c (c may equal grid: one past the end).
+GR_HD int64_t sk_begin(const gemm_relu_plan_t& p, int32_t c) {
+    return (int64_t)c * p.sk_q + (c < p.sk_r ? c : p.sk_r);
+}
+
+// CTA that owns stream-K unit x.
+GR_HD int32_t sk_owner(const gemm_relu_plan_t& p, int64_t x) {
+    const int64_t big = (int64_t)p.sk_r * (p.sk_q + 1);
+    if (x < big) return (int32_t)(x / (p.sk_q + 1));
+    return (int32_t)(p.sk_r + (x - big) / p.sk_q);
+}
+
+struct WorkItem {
+    int32_t tile;      // linear tile id
+    int32_t tm, tn;    // tile row / column
+    int32_t kb0, kb1;  // k-blocks [kb0, kb1)
+    int32_t slot;      // share index within a split tile (0 when whole)
+    int32_t nslots;    // CTAs sharing this tile (1 when whole)
+    int32_t sk_index;  // stream-K tile index (tile - dp_tiles), -1 when data-parallel
+};
+
+struct WorkIter {
+    int32_t cta;
+    int32_t dp_i, dp_n;
+    int64_t u, u1;
+
+    GR_HD void init(const gemm_relu_plan_t& p, int32_t c) {
+        cta = c;
+        dp_i = 0;
+        dp_n = (c < p.dp_tiles) ? (p.dp_tiles - 1 - c) / p.grid + 1 : 0;
+        if (p.sk_tiles > 0) {
+            u = sk_begin(p, c);
+            u1 = sk_begin(p, c + 1);
+        } else {
+            u = u1 = 0;
+        }
+    }
+
+    GR_HD bool next(const gemm_relu_plan_t& p, WorkItem& w) {
+        if (dp_i < dp_n) {
+            w.tile = cta + dp_i * p.grid;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.slot = 0;
+            w.nslots = 1;
+            w.sk_index = -1;
+            ++dp_i;
+            tile_coords(p, w.tile, w.tm, w.tn);
+            return true;
+        }
+        if (u < u1) {
+            const int64_t t = u / p.num_kb;
+            const int32_t kb0 = (int32_t)(u - t * p.num_kb);
+            const int64_t left = u1 - u;
+            const int32_t kb1 = (int64_t)(p.num_kb - kb0) < left ? p.num_kb : kb0 + (int32_t)left;
+            const int32_t first = sk_owner(p, t * p.num_kb);
+            const int32_t last = sk_owner(p, (t + 1) * p.num_kb - 1);
+            w.sk_index = (int32_t)t;
+            w.tile = p.dp_tiles + (int32_t)t;
+            w.kb0 = kb0;
+            w.kb1 = kb1;
+            w.slot = cta - first;
+            w.nslots = last - first + 1;
+            u += kb1 - kb0;
+            tile_coords(p, w.tile, w.tm, w.tn);
+            return true;
+        }
+        return false;
+    }
+};
+
+}  // namespace gr
