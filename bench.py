@@ -197,7 +197,7 @@ def time_device(w, device, steps, warmup, world):
     barrier(world)
     torch.cuda.synchronize(device)
     # keep the device busy while the launches are queued
-    torch.cuda._sleep(int(max(2_000_000, steps * 120_000)))
+    torch.cuda._sleep(int(max(4_000_000, steps * 1_000_000)))
     for i in range(steps):
         a, b, c = sets[i % len(sets)]
         starts[i].record(stream)
@@ -433,6 +433,25 @@ def run_ours(args, w):
     return 0
 
 
+def run_profile_launches(args, w):
+    """A few launches on one input set, for an ncu capture (no timing)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from tiled_dense_gemm_gb300 import binding
+    from tiled_dense_gemm_gb300.workloads import workload_inputs
+    device = torch.device("cuda", 0)
+    A, B = workload_inputs(w)
+    a, b = A.to(device), B.to(device)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+    for _ in range(args.ncu_launches):
+        binding.gemm_relu(a, b, c, True)
+    binding.check_device_error()
+    torch.cuda.synchronize(device)
+    print(f"profile launches done: {args.ncu_launches} x {w.name}")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,6 +463,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-extra", action="store_true", help="skip the 4096^3 and skinny side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--ncu-launches", type=int, default=0,
+                    help="profiling mode: run only this many launches of the workload and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -451,6 +472,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.ncu_launches:
+        return run_profile_launches(args, w)
     return run_ours(args, w)
 
 
