@@ -94,15 +94,17 @@ void gemm_relu_shutdown(void);
 /* ---- Host-only planning interface (no CUDA calls; usable without a GPU) -- */
 
 typedef struct {
-    int32_t path;        /* 0 nothing to do, 1 zero fill (K == 0), 2 tiled, 3 swapped operands */
-    int32_t mma_m;       /* tcgen05 MMA M: 128 (C rows for path 2, C columns for path 3) */
+    int32_t path;        /* 0 nothing to do, 1 zero fill (K == 0), 2 tiled (one CTA per tile),
+                            3 swapped operands (small M), 4 tiled by CTA pairs (256 x 256) */
+    int32_t mma_m;       /* tcgen05 MMA M: 128, or 256 for a CTA pair (C rows; C columns for path 3) */
     int32_t mma_n;       /* tcgen05 MMA N: 128 or 256 (C columns) / padded M (path 3) */
     int32_t tile_m;      /* C tile rows */
     int32_t tile_n;      /* C tile columns */
     int32_t tiles_m, tiles_n, num_tiles;
     int32_t num_kb;      /* ceil(K / 64) */
     int32_t group_m;     /* tile rasterisation: tiles_m are walked in groups of group_m */
-    int32_t grid;        /* persistent CTAs */
+    int32_t grid;        /* persistent workers (a worker is `cluster` CTAs) */
+    int32_t cluster;     /* CTAs per worker: 1, or 2 for path 4 */
     int32_t dp_tiles;    /* tiles [0, dp_tiles) are done whole, round-robin over CTAs */
     int32_t sk_tiles;    /* tiles [dp_tiles, num_tiles) are split along K (stream-K) */
     int32_t sk_q, sk_r;  /* stream-K k-blocks per CTA: q, plus 1 for CTAs < r */
@@ -112,18 +114,23 @@ typedef struct {
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
-    int64_t counter_count;   /* arrival counters (one per stream-K tile) */
+    int64_t counter_count;   /* arrival counters (one per stream-K tile and CTA of a worker) */
 } gemm_relu_plan_t;
 
 /*
  * Fills *plan with the decomposition gemm_relu uses for an M x N x K
- * problem on a device with `num_sms` multiprocessors.  Pure host code.
+ * problem on a device with `num_sms` multiprocessors (CTA pairs: at most
+ * num_sms / 2; the runtime also caps them by the device's co-resident
+ * cluster count).  Pure host code.  The environment variable
+ * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
+ * "tiled256", "tiled128", "swap" (M <= 128 only) or "pair", optionally
+ * followed by ":dp" to forbid splitting tiles along K.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);
 
 /*
- * The idx-th work item of CTA `cta` under *plan, exactly as the kernel walks
+ * The idx-th work item of worker `cta` under *plan, exactly as the kernel walks
  * it: C tile `tile` (tile_m_idx, tile_n_idx after rasterisation), k-blocks
  * [kb_begin, kb_end), and for a tile split along K its share `slot` of
  * `nslots`.  Returns 1 if the item exists, 0 past the CTA's last item,

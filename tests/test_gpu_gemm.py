@@ -253,3 +253,24 @@ def test_stream_k_counters_are_left_zero():
         c = binding.gemm_relu(a, b)
     binding.check_device_error()
     assert_close(c.cpu(), ref, "after repeats")
+
+
+# ---------------------------------------------------------------- every kernel shape
+
+FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (1024, 1024, 1024),
+                 (257, 1032, 4104), (96, 2048, 3000)]
+
+
+@pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "tiled128:dp",
+                                   "pair:dp", "swap", "swap:dp"])
+def test_each_kernel_shape_parity(monkeypatch, force):
+    """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
+    swapped operands), with and without stream-K splitting, on ragged shapes."""
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    for M, N, K in FORCED_SHAPES:
+        A, B = make_inputs(M, N, K, seed=M + N + K, dist_a="uniform", dist_b="uniform")
+        for relu in (True, False):
+            C = gpu_run(A, B, relu)
+            ref = oracle.gemm_relu(A, B, relu, threads=THREADS)
+            assert_close(C, ref, f"{force} {M}x{N}x{K} relu={relu}")
+            assert_relu_sign(C, relu)

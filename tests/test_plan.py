@@ -21,24 +21,34 @@ SHAPES = [(w.M, w.N, w.K) for w in WORKLOADS.values()] + [
 ]
 
 
-def _check(gemm_lib, M, N, K, sms):
+def _check(gemm_lib, M, N, K, sms, forced=False):
     p = gemm_lib.plan(M, N, K, sms)
     d = p.as_dict()
-    assert d["path"] == (3 if M <= 128 else 2)
-    assert d["mma_m"] == 128
+    if forced:
+        assert d["path"] in (2, 3, 4)
+    elif M <= 128:
+        assert d["path"] == 3
+    else:
+        assert d["path"] in (2, 4)
     if d["path"] == 3:
         assert d["mma_n"] == ((M + 15) // 16) * 16 and d["tile_n"] == 128
-    else:
+        assert d["mma_m"] == 128 and d["cluster"] == 1
+    elif d["path"] == 2:
         assert d["mma_n"] in (128, 256) and d["tile_m"] == 128
+        assert d["mma_m"] == 128 and d["cluster"] == 1
+    else:
+        assert (d["mma_m"], d["mma_n"], d["tile_m"], d["tile_n"], d["cluster"]) == (256, 256, 256, 256, 2)
+        assert d["stage_bytes"] == 32768
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
     assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
     assert d["num_kb"] == (K + 63) // 64
     assert 2 <= d["num_stages"] <= 16
     assert d["smem_bytes"] <= SMEM_LIMIT
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
-    assert 1 <= d["grid"] <= sms
+    assert 1 <= d["grid"] * d["cluster"] <= sms
     assert d["dp_tiles"] + d["sk_tiles"] == d["num_tiles"]
-    assert d["workspace_bytes"] == d["sk_tiles"] * d["max_slots"] * 128 * d["mma_n"] * 4
+    assert d["workspace_bytes"] == d["sk_tiles"] * d["cluster"] * d["max_slots"] * 128 * d["mma_n"] * 4
+    assert d["counter_count"] == d["sk_tiles"] * d["cluster"]
 
     cover = defaultdict(int)
     slots = defaultdict(dict)
@@ -92,6 +102,21 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
     _check(gemm_lib, *shape, sms)
 
 
+@pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
+                                   "swap", "swap:dp"])
+def test_forced_paths(gemm_lib, monkeypatch, force):
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256)}
+    for shape in SHAPES:
+        d = _check(gemm_lib, *shape, 152, forced=True)
+        if force.startswith("swap"):
+            assert d["path"] == (3 if shape[0] <= 128 else d["path"])
+        else:
+            assert (d["path"], d["mma_n"]) == want[force.split(":")[0]]
+        if force.endswith(":dp"):
+            assert d["sk_tiles"] == 0
+
+
 def test_random_shapes(gemm_lib):
     rng = random.Random(0)
     for _ in range(60):
@@ -113,6 +138,6 @@ def test_degenerate_plans(gemm_lib):
 
 def test_headline_shapes_use_the_intended_kernels(gemm_lib):
     sq = gemm_lib.plan(4096, 4096, 4096, 152)
-    assert sq.path == 2 and sq.grid == 152
+    assert sq.path == 4 and sq.grid == 76 and sq.cluster == 2
     sk = gemm_lib.plan(16, 8192, 8192, 152)
     assert sk.path == 3 and sk.mma_n == 16 and sk.grid == 152 and sk.sk_tiles == sk.num_tiles

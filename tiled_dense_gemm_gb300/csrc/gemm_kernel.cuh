@@ -1,6 +1,7 @@
 // Persistent, warp-specialised C = ReLU(A . B) kernel for sm_103a.
 //
-// Per CTA (192 threads, one CTA per SM):
+// Per CTA (192 threads, one CTA per SM; in the paired mode two CTAs on two
+// SMs form a cluster and share each MMA, tcgen05 cta_group::2):
 //   warp 0      TMA producer: one thread streams A and B k-blocks into a
 //               ring of shared-memory stages (128-byte swizzle), each stage
 //               guarded by a full/empty mbarrier pair;
@@ -75,11 +76,17 @@ struct KParams {
 };
 
 // kMode 0: C tile 128 x 256; 1: C tile 128 x 128; 2: swapped operands
-// (C tile mpad x 128: B^T is the MMA A operand, A^T the MMA B operand).
+// (C tile mpad x 128: B^T is the MMA A operand, A^T the MMA B operand);
+// 3: CTA pair, C tile 256 x 256 (each CTA holds 128 rows of A, 128 columns
+// of B, and accumulates its 128 rows x 256 columns).
 template <int kMode>
 struct ModeTraits {
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr uint32_t kBN = (kMode == 0) ? 256 : 128;  // C columns per tile (normal)
+    static constexpr bool kPair = (kMode == 3);
+    static constexpr int kCG = kPair ? 2 : 1;
+    static constexpr uint32_t kBN = (kMode == 1) ? 128 : 256;  // C columns per tile (normal)
+    static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
+    static constexpr uint32_t kBCols = kPair ? 128 : kBN;      // B columns loaded per CTA
     static constexpr int kCols = kSwap ? 16 : 32;              // TMEM columns per epilogue load
 };
 
@@ -125,12 +132,12 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 
 template <int kMode>
 __device__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
-                              const CUtensorMap* tmA, const CUtensorMap* tmB) {
+                              const CUtensorMap* tmA, const CUtensorMap* tmB, int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t& pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
     WorkIter wi;
-    wi.init(pl, blockIdx.x);
+    wi.init(pl, worker);
     WorkItem w;
     uint32_t it = 0;
     while (wi.next(pl, w)) {
@@ -142,16 +149,29 @@ __device__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uin
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + kOperandA;
             const int32_t k0 = kb * kBlockK;
-            mbar_arrive_expect_tx(full, (uint32_t)pl.stage_bytes);
-            if constexpr (!T::kSwap) {
-                tma_load_2d(a_dst, tmA, full, k0, w.tm * 128);
+            if constexpr (T::kPair) {
+                // both CTAs' copies complete on the leader's barrier, which
+                // expects the bytes of the pair
+                const uint32_t rank = cluster_ctarank();
+                const uint32_t full_leader = mapa_shared(full, 0);
+                if (rank == 0) mbar_arrive_expect_tx(full, 2u * (uint32_t)pl.stage_bytes);
+                tma_load_2d_pair(a_dst, tmA, full_leader, k0, w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank);
 #pragma unroll
-                for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                    tma_load_2d(b_dst + j * kChunkBytes, tmB, full, w.tn * (int32_t)T::kBN + 64 * j, k0);
+                for (uint32_t j = 0; j < T::kBCols / 64; ++j)
+                    tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader,
+                                     w.tn * (int32_t)T::kBN + 128 * (int32_t)rank + 64 * j, k0);
             } else {
-                tma_load_2d(a_dst, tmB, full, w.tn * 128, k0);
-                tma_load_2d(a_dst + kChunkBytes, tmB, full, w.tn * 128 + 64, k0);
-                tma_load_2d(b_dst, tmA, full, k0, w.tm * pl.tile_m);
+                mbar_arrive_expect_tx(full, (uint32_t)pl.stage_bytes);
+                if constexpr (!T::kSwap) {
+                    tma_load_2d(a_dst, tmA, full, k0, w.tm * 128);
+#pragma unroll
+                    for (uint32_t j = 0; j < T::kBN / 64; ++j)
+                        tma_load_2d(b_dst + j * kChunkBytes, tmB, full, w.tn * (int32_t)T::kBN + 64 * j, k0);
+                } else {
+                    tma_load_2d(a_dst, tmB, full, w.tn * 128, k0);
+                    tma_load_2d(a_dst + kChunkBytes, tmB, full, w.tn * 128 + 64, k0);
+                    tma_load_2d(b_dst, tmA, full, k0, w.tm * pl.tile_m);
+                }
             }
         }
     }
@@ -159,13 +179,13 @@ __device__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uin
 
 template <int kMode>
 __device__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
-                         uint32_t tmem_base) {
+                         uint32_t tmem_base, int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t& pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     WorkIter wi;
-    wi.init(pl, blockIdx.x);
+    wi.init(pl, worker);
     WorkItem w;
     uint32_t it = 0, local = 0;
     while (wi.next(pl, w)) {
@@ -193,11 +213,12 @@ __device__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t
                     adesc = make_sw128_desc(a_base + k * 2 * kAtomBytes, kChunkBytes, kAtomBytes);
                     bdesc = make_sw128_desc(b_base + k * 32, 16, kAtomBytes);
                 }
-                mma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                mma_f16_ss<T::kCG>(d_tmem, adesc, bdesc, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(smem_u32(&ctrl->empty[s]));  // stage free once these MMAs are done
+            // stage free (in both CTAs of a pair) once these MMAs are done
+            mma_commit<T::kCG>(smem_u32(&ctrl->empty[s]), 0x3);
         }
-        mma_commit(smem_u32(&ctrl->tmem_full[buf]));  // accumulator ready
+        mma_commit<T::kCG>(smem_u32(&ctrl->tmem_full[buf]), 0x3);  // accumulator ready
         ++local;
     }
 }
@@ -209,7 +230,7 @@ __device__ __forceinline__ void store_chunk(const KParams& p, const WorkItem& w,
                                             uint32_t col0, const float* v) {
     using T = ModeTraits<kMode>;
     if constexpr (!T::kSwap) {
-        const int64_t m = (int64_t)w.tm * 128 + lane_row;
+        const int64_t m = (int64_t)w.tm * T::kTileM + lane_row;  // lane_row includes the pair half
         if (m >= p.M) return;
         const int64_t n0 = (int64_t)w.tn * T::kBN + col0;
         __half* dst = p.C + m * p.N + n0;
@@ -247,18 +268,20 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
 }
 
 template <int kMode>
-__device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base) {
+__device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base, int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t& pl = p.plan;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
-    const uint32_t lane_row = quarter * 32 + lane;
+    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
+    const uint32_t lane_row = quarter * 32 + lane;             // TMEM lane = accumulator row
+    const uint32_t out_row = lane_row + 128u * rank;           // row within the C tile
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
     const int64_t tile_elems = (int64_t)128 * ncols;
     volatile int32_t* last_flag = &ctrl->last_flag;
     WorkIter wi;
-    wi.init(pl, blockIdx.x);
+    wi.init(pl, worker);
     WorkItem w;
     uint32_t local = 0;
     float v[T::kCols];
@@ -270,14 +293,15 @@ __device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base) 
         if (!ok) return;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + buf * cols_per_buf;
+        // partial tiles are kept per CTA (one per pair half)
+        const int64_t split_id = T::kPair ? (int64_t)w.sk_index * 2 + rank : (int64_t)w.sk_index;
         float* part = nullptr;
-        if (w.nslots > 1)
-            part = p.ws + ((int64_t)w.sk_index * pl.max_slots + w.slot) * tile_elems;
+        if (w.nslots > 1) part = p.ws + (split_id * pl.max_slots + w.slot) * tile_elems;
         for (uint32_t c = 0; c < ncols; c += T::kCols) {
             __syncwarp();  // tcgen05.ld is warp-collective
             tmem_load_chunk<kMode>(taddr + c, v);
             if (w.nslots == 1) {
-                store_chunk<kMode>(p, w, lane_row, c, v);
+                store_chunk<kMode>(p, w, out_row, c, v);
             } else {
 #pragma unroll
                 for (int j = 0; j < T::kCols; ++j) __stcg(part + (int64_t)(c + j) * 128 + lane_row, v[j]);
@@ -286,21 +310,26 @@ __device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base) 
         // accumulator buffer back to the MMA warp
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
+        if (lane == 0) {
+            if constexpr (T::kPair)
+                mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->tmem_empty[buf]), 0));
+            else
+                mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
+        }
         if (w.nslots > 1) {
             // publish the partial, count arrivals; the last CTA reduces
             __threadfence();
             named_bar_sync(kEpiBarrier, kEpiThreads);
             if (threadIdx.x == 64) {
-                const uint32_t prev = atomicAdd(&p.counters[w.sk_index], 1u);
+                const uint32_t prev = atomicAdd(&p.counters[split_id], 1u);
                 const int32_t last = (prev == (uint32_t)(w.nslots - 1)) ? 1 : 0;
-                if (last) p.counters[w.sk_index] = 0u;  // ready for the next launch
+                if (last) p.counters[split_id] = 0u;  // ready for the next launch
                 *last_flag = last;
             }
             named_bar_sync(kEpiBarrier, kEpiThreads);
             if (*last_flag) {
                 __threadfence();
-                const float* base = p.ws + (int64_t)w.sk_index * pl.max_slots * tile_elems;
+                const float* base = p.ws + split_id * pl.max_slots * tile_elems;
                 for (uint32_t c = 0; c < ncols; c += T::kCols) {
 #pragma unroll
                     for (int j = 0; j < T::kCols; ++j) v[j] = 0.0f;
@@ -309,7 +338,7 @@ __device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base) 
 #pragma unroll
                         for (int j = 0; j < T::kCols; ++j) v[j] += __ldcg(src + (int64_t)j * 128);
                     }
-                    store_chunk<kMode>(p, w, lane_row, c, v);
+                    store_chunk<kMode>(p, w, out_row, c, v);
                 }
             }
         }
@@ -323,15 +352,19 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ KParams p) {
+    using T = ModeTraits<kMode>;
     extern __shared__ __align__(1024) uint8_t smem[];
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
     const uint32_t base = smem_u32(smem);
     const uint32_t stages = (base + (uint32_t)sizeof(Ctrl) + 1023u) & ~1023u;
     const gemm_relu_plan_t& pl = p.plan;
     const uint32_t a_bytes = kOperandA;
-    const uint32_t b_bytes = ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u;
+    const uint32_t b_bytes = (T::kPair ? T::kBCols * kBlockK * 2
+                                       : ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
+    const int32_t worker = T::kPair ? (int32_t)(blockIdx.x / 2) : (int32_t)blockIdx.x;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -342,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);
-            mbar_init(smem_u32(&ctrl->tmem_empty[b]), kEpiThreads / 32);
+            // a pair's leader also counts the peer's epilogue warps
+            mbar_init(smem_u32(&ctrl->tmem_empty[b]), (T::kPair ? 2u : 1u) * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctrl->final_bar), 1);
         ctrl->abort_flag = 0;
@@ -350,27 +384,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
-        tmem_relinquish();
+        tmem_alloc<T::kCG>(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
+        tmem_relinquish<T::kCG>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (T::kPair)
+        cluster_sync();  // the peer's barriers are initialised before any remote arrive
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_addr;
 
     if (warp == 0) {
-        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, &tmA, &tmB);
+        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, &tmA, &tmB, worker);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
-            mma_role<kMode>(p, ctrl, stages, stride, tmem_base);
-            // no MMA may still be writing TMEM when it is released
-            mma_commit(smem_u32(&ctrl->final_bar));
+        if (lane == 0 && rank == 0) {  // one thread of the (leader) CTA issues every MMA
+            mma_role<kMode>(p, ctrl, stages, stride, tmem_base, worker);
+            // no MMA may still be running when tensor memory is released
+            mma_commit<T::kCG>(smem_u32(&ctrl->final_bar), 0x1);
             if (!wait_phase_for(smem_u32(&ctrl->final_bar), 0, p.timeout_ns)) atomicCAS(p.err, 0, kErrFinal);
         }
         __syncwarp();
     } else {
-        epilogue_role<kMode>(p, ctrl, tmem_base);
+        epilogue_role<kMode>(p, ctrl, tmem_base, worker);
     }
 
     if (warp == 0 && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
@@ -381,10 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (T::kPair)
+        cluster_sync();  // the peer's shared memory is read by the pair's MMAs until here
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, (uint32_t)pl.tmem_cols);
+        tmem_dealloc<T::kCG>(tmem_base, (uint32_t)pl.tmem_cols);
     }
 }
 

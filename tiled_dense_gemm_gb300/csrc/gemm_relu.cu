@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -35,8 +36,9 @@ struct DeviceState {
     bool inited = false;
     int status = GEMM_OK;
     int sm_count = 0;
+    int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[3] = {false, false, false};
+    bool attr_set[4] = {false, false, false, false};
     std::vector<StreamBuffers> streams;
 };
 
@@ -83,6 +85,32 @@ int init_device_locked(int dev) {
             return d.status = GEMM_ERR_UNSUPPORTED_DEVICE;
         }
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    {
+        // how many CTA pairs of the paired kernel can be resident at once
+        auto fn = gemm_relu_kernel<3>;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) ==
+            cudaSuccess) {
+            d.attr_set[3] = true;
+            gemm_relu_plan_t probe;
+            plan_problem(4096, 4096, 4096, d.sm_count, 0, "pair", &probe);
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = (size_t)probe.smem_bytes;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) d.max_pairs = n;
+        }
+        cudaGetLastError();
+        // no co-resident pairs reported: the paired kernel is not used
+        if (d.max_pairs <= 0) d.max_pairs = -1;
     }
     if (cudaMalloc(&d.d_err, 16) != cudaSuccess) {
         cudaGetLastError();
@@ -163,7 +191,24 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
         }
         d.attr_set[kMode] = true;
     }
-    fn<<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, kp);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(pl.grid * pl.cluster), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+    cfg.stream = st;
+    if (pl.cluster > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)pl.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, kp) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
@@ -196,14 +241,19 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_LAUNCH;
     }
     gemm_relu_plan_t pl;
-    {
+    const char* force = getenv("GEMM_RELU_FORCE_PATH");
+    if (force && *force) {
+        // tuning / test override: plan every call, bypass the cache
+        int rc = plan_problem(M, N, K, d.sm_count, d.max_pairs, force, &pl);
+        if (rc != GEMM_OK) return rc;
+    } else {
         auto& cache = g_plans[dev];
         PlanKey key{M, N, K};
         auto itp = cache.find(key);
         if (itp != cache.end()) {
             pl = itp->second;
         } else {
-            int rc = gemm_relu_plan(M, N, K, d.sm_count, &pl);
+            int rc = plan_problem(M, N, K, d.sm_count, d.max_pairs, nullptr, &pl);
             if (rc != GEMM_OK) return rc;
             if (cache.size() > 4096) cache.clear();
             cache.emplace(key, pl);
@@ -240,7 +290,8 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
         return launch_mode<2>(d, pl, kp, ta, tb, st);
     }
-    kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);
+    kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);
+    if (pl.path == 4) return launch_mode<3>(d, pl, kp, ta, tb, st);
     if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, st);
     return launch_mode<1>(d, pl, kp, ta, tb, st);
 }

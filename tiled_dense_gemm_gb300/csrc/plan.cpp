@@ -2,6 +2,7 @@
 // stream-K split for one problem size, by a small cost model evaluated
 // over the exact work lists the kernel will walk.  Pure host code.
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "gemm_relu.h"
@@ -28,8 +29,11 @@ struct Costs {
 
 static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     Costs c;
-    const double tile_elems = 128.0 * mma_n;
-    if (path == 2) {
+    const double tile_elems = 128.0 * mma_n;  // per CTA
+    if (path == 4) {
+        // a CTA pair: each CTA's tensor core does 128 x 256 x 64 per k-block
+        c.kb = 4.0 * 128.0 * 256.0 * 16.0 * 2.0 / 8192.0;
+    } else if (path == 2) {
         // 4 MMAs of 128 x N x 16 per k-block; the tensor pipe does
         // 8192 fp16 FLOP per SM per clock.  N = 128 is also bound by
         // shared-memory bandwidth, hence the extra factor.
@@ -103,18 +107,23 @@ static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t 
         p.sk_q = p.sk_r = 0;
         p.max_slots = 1;
     }
-    p.workspace_bytes = (int64_t)sk * p.max_slots * p.mma_m * p.mma_n * 4;
-    p.counter_count = sk;
+    // one fp32 partial of 128 rows x mma_n columns per (tile, CTA of the worker, slot)
+    p.workspace_bytes = (int64_t)sk * p.cluster * p.max_slots * 128 * p.mma_n * 4;
+    p.counter_count = (int64_t)sk * p.cluster;
 }
 
 // Fill the shape-dependent fields for one kernel shape.
 static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path,
                        int32_t mma_n) {
     p.path = path;
-    p.mma_m = 128;
     p.mma_n = mma_n;
+    p.cluster = (path == 4) ? 2 : 1;
+    p.mma_m = (path == 4) ? 256 : 128;
     if (path == 2) {
         p.tile_m = 128;
+        p.tile_n = mma_n;
+    } else if (path == 4) {
+        p.tile_m = 256;
         p.tile_n = mma_n;
     } else {
         p.tile_m = mma_n;  // padded M
@@ -125,7 +134,9 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = (int32_t)((K + kBlockK - 1) / kBlockK);
     p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
-    const int32_t b_bytes = mma_n * kBlockK * 2;
+    // per CTA: B columns it loads (half of the tile for a pair)
+    const int32_t b_cols = (path == 4) ? mma_n / 2 : mma_n;
+    const int32_t b_bytes = b_cols * kBlockK * 2;
     p.stage_bytes = kOperandABytes + b_bytes;
     const int32_t stride = kOperandABytes + ((b_bytes + 1023) / 1024) * 1024;
     int32_t stages = kStageBudget / stride;
@@ -138,8 +149,9 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     p.tmem_cols = alloc;
 }
 
-// Choose the best split for the current shape; returns its estimated cost.
-static double choose_split(gemm_relu_plan_t& p, int32_t sms) {
+// Choose the best split for the current shape over at most `workers`
+// persistent workers; returns its estimated cost.
+static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only) {
     const Costs c = costs_for(p.path, p.mma_n, p.stage_bytes);
     const int32_t T = p.num_tiles;
     gemm_relu_plan_t best = p;
@@ -158,23 +170,34 @@ static double choose_split(gemm_relu_plan_t& p, int32_t sms) {
         }
     };
     // plain data-parallel
-    consider(T < sms ? T : sms, T, 0);
-    if (T >= sms) {
-        const int32_t full = T / sms;
-        if (T % sms != 0) consider(sms, (full - 1) * sms, T - (full - 1) * sms);
-    } else if (p.num_kb > 1) {
-        // fewer tiles than SMs: split every tile along K over more CTAs
-        for (int32_t g = T + 1; g <= sms; ++g) consider(g, 0, T);
+    consider(T < workers ? T : workers, T, 0);
+    if (!dp_only) {
+        if (T >= workers) {
+            const int32_t full = T / workers;
+            if (T % workers != 0) consider(workers, (full - 1) * workers, T - (full - 1) * workers);
+        } else if (p.num_kb > 1) {
+            // fewer tiles than workers: split every tile along K over more workers
+            for (int32_t g = T + 1; g <= workers; ++g) consider(g, 0, T);
+        }
     }
     p = best;
     return best_cost;
 }
 
-}  // namespace gr
+static bool starts_with(const char* s, const char* prefix) {
+    while (*prefix)
+        if (*s++ != *prefix++) return false;
+    return true;
+}
 
-extern "C" int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms,
-                              gemm_relu_plan_t* plan) {
-    using namespace gr;
+static bool contains(const char* s, const char* what) {
+    for (; *s; ++s)
+        if (starts_with(s, what)) return true;
+    return false;
+}
+
+int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, const char* force,
+                 gemm_relu_plan_t* plan) {
     if (!plan || M < 0 || N < 0 || K < 0 || M > GEMM_RELU_MAX_DIM || N > GEMM_RELU_MAX_DIM ||
         K > GEMM_RELU_MAX_DIM || num_sms < 1)
         return GEMM_ERR_INVALID_ARG;
@@ -192,23 +215,52 @@ extern "C" int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms,
     const int64_t tiles_small = ((M + 127) / 128) * ((N + 127) / 128);
     if (tiles_small > (int64_t)1 << 30 || kb > (int64_t)1 << 30) return GEMM_ERR_INVALID_ARG;
 
-    if (M <= 128) {
+    const char* f = force ? force : "";
+    const bool dp_only = contains(f, ":dp");
+    int32_t pairs = (max_pairs > 0 && max_pairs < num_sms / 2) ? max_pairs : num_sms / 2;
+
+    bool want_swap = M <= 128, want_t256 = M > 128, want_t128 = M > 128, want_pair = M > 128 && pairs > 0;
+    if (starts_with(f, "swap") && M <= 128) {
+        want_t256 = want_t128 = want_pair = false;
+        want_swap = true;
+    } else if (starts_with(f, "tiled256")) {
+        want_swap = want_t128 = want_pair = false;
+        want_t256 = true;
+    } else if (starts_with(f, "tiled128")) {
+        want_swap = want_t256 = want_pair = false;
+        want_t128 = true;
+    } else if (starts_with(f, "pair") && pairs > 0) {
+        want_swap = want_t256 = want_t128 = false;
+        want_pair = true;
+    }
+
+    double best_cost = -1.0;
+    auto take = [&](int32_t path, int32_t mma_n, int32_t workers) {
+        gemm_relu_plan_t q;
+        memset(&q, 0, sizeof(q));
+        shape_plan(q, M, N, K, path, mma_n);
+        const double cost = choose_split(q, workers, dp_only);
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
+            *plan = q;
+        }
+    };
+    if (want_swap) {
         // small M: C^T = B^T A^T, so N runs along the 128-wide MMA M side
         // and M (padded to 16) is the MMA N side.
-        const int32_t mpad = (int32_t)((M + 15) / 16) * 16;
-        shape_plan(*plan, M, N, K, 3, mpad);
-        choose_split(*plan, num_sms);
-        return GEMM_OK;
+        take(3, (int32_t)((M + 15) / 16) * 16, num_sms);
     }
-    gemm_relu_plan_t a, b;
-    memset(&a, 0, sizeof(a));
-    memset(&b, 0, sizeof(b));
-    shape_plan(a, M, N, K, 2, 256);
-    shape_plan(b, M, N, K, 2, 128);
-    const double ca = choose_split(a, num_sms);
-    const double cb = choose_split(b, num_sms);
-    *plan = (cb < ca) ? b : a;
+    if (want_pair) take(4, 256, pairs);
+    if (want_t256) take(2, 256, num_sms);
+    if (want_t128) take(2, 128, num_sms);
     return GEMM_OK;
+}
+
+}  // namespace gr
+
+extern "C" int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms,
+                              gemm_relu_plan_t* plan) {
+    return gr::plan_problem(M, N, K, num_sms, 0, getenv("GEMM_RELU_FORCE_PATH"), plan);
 }
 
 extern "C" int gemm_relu_plan_work_item(const gemm_relu_plan_t* plan, int cta, int idx,

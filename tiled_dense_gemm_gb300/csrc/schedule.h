@@ -115,4 +115,10 @@ struct WorkIter {
     }
 };
 
+// Planner with the runtime's limits: at most `max_pairs` co-resident CTA
+// pairs (<= 0: num_sms / 2).  `force` is the GEMM_RELU_FORCE_PATH value or
+// nullptr.  Defined in plan.cpp.
+int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, const char* force,
+                 gemm_relu_plan_t* plan);
+
 }  // namespace gr
