@@ -129,96 +129,132 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 }
 
 // ------------------------------------------------------------------ roles
+//
+// The producer and MMA roles are single threads whose k-block loop is on
+// the critical path of the tensor pipe: every instruction latency in it is
+// exposed.  So the loop runs from registers only: the plan is copied once,
+// ring stage / phase advance without division, barrier addresses are base +
+// 8 * stage, and shared-memory descriptors are built once and advanced by
+// adding to their start-address field (a 14-bit field of 16-byte units that
+// cannot carry: shared addresses stay below 256 KiB).
 
 template <int kMode>
-__device__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
-                              const CUtensorMap* tmA, const CUtensorMap* tmB, int32_t worker) {
+__device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
+                                              uint32_t stride, const CUtensorMap* tmA,
+                                              const CUtensorMap* tmB, int32_t worker) {
     using T = ModeTraits<kMode>;
-    const gemm_relu_plan_t& pl = p.plan;
+    const gemm_relu_plan_t pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
+    const uint32_t full0 = smem_u32(&ctrl->full[0]);
+    const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
+    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
+    // a pair's copies all complete on the leader's barrier, which expects
+    // the bytes of both CTAs
+    const uint32_t tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
+    const int32_t tile_m = pl.tile_m;
     WorkIter wi;
     wi.init(pl, worker);
     WorkItem w;
-    uint32_t it = 0;
+    uint32_t s = 0, ph = 0;
     while (wi.next(pl, w)) {
-        for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-            const uint32_t s = it % S;
-            const uint32_t ph = (it / S) & 1u;
-            if (!wait_phase(smem_u32(&ctrl->empty[s]), ph ^ 1u, ctrl, p, kErrProducer)) return;
-            const uint32_t full = smem_u32(&ctrl->full[s]);
+        // first row of A and first column of B this CTA loads for the tile
+        int32_t a_row, b_col;
+        if constexpr (T::kPair) {
+            a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
+            b_col = w.tn * (int32_t)T::kBN + 128 * (int32_t)rank;
+        } else if constexpr (!T::kSwap) {
+            a_row = w.tm * 128;
+            b_col = w.tn * (int32_t)T::kBN;
+        } else {
+            a_row = w.tm * tile_m;
+            b_col = w.tn * 128;
+        }
+        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return;
+            const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + kOperandA;
             const int32_t k0 = kb * kBlockK;
             if constexpr (T::kPair) {
-                // both CTAs' copies complete on the leader's barrier, which
-                // expects the bytes of the pair
-                const uint32_t rank = cluster_ctarank();
                 const uint32_t full_leader = mapa_shared(full, 0);
-                if (rank == 0) mbar_arrive_expect_tx(full, 2u * (uint32_t)pl.stage_bytes);
-                tma_load_2d_pair(a_dst, tmA, full_leader, k0, w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank);
+                if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
+                tma_load_2d_pair(a_dst, tmA, full_leader, k0, a_row);
 #pragma unroll
                 for (uint32_t j = 0; j < T::kBCols / 64; ++j)
-                    tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader,
-                                     w.tn * (int32_t)T::kBN + 128 * (int32_t)rank + 64 * j, k0);
+                    tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
             } else {
-                mbar_arrive_expect_tx(full, (uint32_t)pl.stage_bytes);
+                mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
-                    tma_load_2d(a_dst, tmA, full, k0, w.tm * 128);
+                    tma_load_2d(a_dst, tmA, full, k0, a_row);
 #pragma unroll
                     for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                        tma_load_2d(b_dst + j * kChunkBytes, tmB, full, w.tn * (int32_t)T::kBN + 64 * j, k0);
+                        tma_load_2d(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0);
                 } else {
-                    tma_load_2d(a_dst, tmB, full, w.tn * 128, k0);
-                    tma_load_2d(a_dst + kChunkBytes, tmB, full, w.tn * 128 + 64, k0);
-                    tma_load_2d(b_dst, tmA, full, k0, w.tm * pl.tile_m);
+                    // MMA A operand: 128 columns of B (two 64-wide chunks)
+                    tma_load_2d(a_dst, tmB, full, b_col, k0);
+                    tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
+                    // MMA B operand: the (padded) rows of A
+                    tma_load_2d(b_dst, tmA, full, k0, a_row);
                 }
+            }
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
             }
         }
     }
 }
 
 template <int kMode>
-__device__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages, uint32_t stride,
-                         uint32_t tmem_base, int32_t worker) {
+__device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
+                                         uint32_t stride, uint32_t tmem_base, int32_t worker) {
     using T = ModeTraits<kMode>;
-    const gemm_relu_plan_t& pl = p.plan;
+    const gemm_relu_plan_t pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
+    const uint32_t idesc = p.idesc;
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
+    const uint32_t full0 = smem_u32(&ctrl->full[0]);
+    const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
+    const uint32_t tfull0 = smem_u32(&ctrl->tmem_full[0]);
+    const uint32_t tempty0 = smem_u32(&ctrl->tmem_empty[0]);
+    // Descriptors of stage 0 and per-16-k advances, in 16-byte units.
+    // K-major operand (A; A^T when swapped): +32 bytes inside the swizzled
+    // row.  MN-major operand (B; B^T when swapped): +16 k-rows = 2 atoms.
+    const uint64_t a_desc0 = T::kSwap ? make_sw128_desc(stages, kChunkBytes, kAtomBytes)
+                                      : make_sw128_desc(stages, 16, kAtomBytes);
+    const uint64_t b_desc0 = T::kSwap ? make_sw128_desc(stages + kOperandA, 16, kAtomBytes)
+                                      : make_sw128_desc(stages + kOperandA, kChunkBytes, kAtomBytes);
+    constexpr uint32_t kAStep = (T::kSwap ? 2 * kAtomBytes : 32u) >> 4;
+    constexpr uint32_t kBStep = (T::kSwap ? 32u : 2 * kAtomBytes) >> 4;
+    const uint32_t stride16 = stride >> 4;
     WorkIter wi;
     wi.init(pl, worker);
     WorkItem w;
-    uint32_t it = 0, local = 0;
+    uint32_t s = 0, ph = 0, local = 0;
     while (wi.next(pl, w)) {
         const uint32_t buf = local & 1u;
         const uint32_t bph = (local >> 1) & 1u;
-        if (!wait_phase(smem_u32(&ctrl->tmem_empty[buf]), bph ^ 1u, ctrl, p, kErrMmaAccum)) return;
+        if (!wait_phase(tempty0 + 8u * buf, bph ^ 1u, ctrl, p, kErrMmaAccum)) return;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * cols_per_buf;
-        for (int32_t kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-            const uint32_t s = it % S;
-            const uint32_t ph = (it / S) & 1u;
-            if (!wait_phase(smem_u32(&ctrl->full[s]), ph, ctrl, p, kErrMmaStage)) return;
+        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!wait_phase(full0 + 8u * s, ph, ctrl, p, kErrMmaStage)) return;
             tc_fence_after();
-            const uint32_t a_base = stages + s * stride;
-            const uint32_t b_base = a_base + kOperandA;
+            const uint64_t a_desc = a_desc0 + (uint64_t)(s * stride16);
+            const uint64_t b_desc = b_desc0 + (uint64_t)(s * stride16);
+            const uint32_t acc = (kb > w.kb0) ? 1u : 0u;
 #pragma unroll
-            for (uint32_t k = 0; k < kBlockK / 16; ++k) {
-                uint64_t adesc, bdesc;
-                if constexpr (!T::kSwap) {
-                    // A: K-major, advance 16 k = 32 bytes inside the swizzled row
-                    adesc = make_sw128_desc(a_base + k * 32, 16, kAtomBytes);
-                    // B: N-major, advance 16 k-rows = 2 atoms
-                    bdesc = make_sw128_desc(b_base + k * 2 * kAtomBytes, kChunkBytes, kAtomBytes);
-                } else {
-                    adesc = make_sw128_desc(a_base + k * 2 * kAtomBytes, kChunkBytes, kAtomBytes);
-                    bdesc = make_sw128_desc(b_base + k * 32, 16, kAtomBytes);
-                }
-                mma_f16_ss<T::kCG>(d_tmem, adesc, bdesc, p.idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
-            }
+            for (uint32_t k = 0; k < kBlockK / 16; ++k)
+                mma_f16_ss<T::kCG>(d_tmem, a_desc + k * kAStep, b_desc + k * kBStep, idesc,
+                                   k > 0 ? 1u : acc);
             // stage free (in both CTAs of a pair) once these MMAs are done
-            mma_commit<T::kCG>(smem_u32(&ctrl->empty[s]), 0x3);
+            mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
-        mma_commit<T::kCG>(smem_u32(&ctrl->tmem_full[buf]), 0x3);  // accumulator ready
+        mma_commit<T::kCG>(tfull0 + 8u * buf, 0x3);  // accumulator ready
         ++local;
     }
 }
@@ -268,7 +304,7 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
 }
 
 template <int kMode>
-__device__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base, int32_t worker) {
+__device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base, int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t& pl = p.plan;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
