@@ -108,6 +108,9 @@ typedef struct {
     int32_t dp_tiles;    /* tiles [0, dp_tiles) are done whole, round-robin over CTAs */
     int32_t sk_tiles;    /* tiles [dp_tiles, num_tiles) are split along K (stream-K) */
     int32_t sk_q, sk_r;  /* stream-K k-blocks per CTA: q, plus 1 for CTAs < r */
+    int32_t splits;      /* > 1: tiles [dp_tiles, num_tiles) are instead cut into `splits`
+                            equal K ranges; item i is (tile i % T, K range i / T), T the
+                            number of such tiles, and worker c takes items c, c+grid, ... */
     int32_t max_slots;   /* most CTAs sharing one stream-K tile */
     int32_t num_stages;  /* shared-memory ring depth */
     int32_t stage_bytes; /* bytes of A and B tile per ring stage */
@@ -124,7 +127,8 @@ typedef struct {
  * cluster count).  Pure host code.  The environment variable
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
  * "tiled256", "tiled128", "swap" (M <= 128 only) or "pair", optionally
- * followed by ":dp" to forbid splitting tiles along K.
+ * followed by ":dp" to forbid splitting tiles along K, or by ":sN" to cut
+ * every tile into N equal K ranges (the split schedule).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);

@@ -262,7 +262,7 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "tiled128:dp",
-                                   "pair:dp", "swap", "swap:dp"])
+                                   "pair:dp", "swap", "swap:dp", "swap:s7", "tiled128:s3", "pair:s5"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands), with and without stream-K splitting, on ragged shapes."""

@@ -90,7 +90,7 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
             kb = s[i][1]
         assert kb == d["num_kb"]
     # stream-K runs differ by at most one k-block
-    if sk_units:
+    if sk_units and d["splits"] == 1:
         assert max(sk_units) - min(sk_units) <= 1
         assert sum(sk_units) == d["sk_tiles"] * d["num_kb"]
     return d
@@ -103,7 +103,7 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
-                                   "swap", "swap:dp"])
+                                   "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256)}
@@ -115,6 +115,10 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert (d["path"], d["mma_n"]) == want[force.split(":")[0]]
         if force.endswith(":dp"):
             assert d["sk_tiles"] == 0
+        if ":s" in force:
+            want_s = min(int(force.split(":s")[1]), d["num_kb"])
+            assert d["dp_tiles"] == 0 and d["max_slots"] == want_s
+            assert d["splits"] == (want_s if want_s > 1 else 1)
 
 
 def test_random_shapes(gemm_lib):

@@ -32,7 +32,7 @@ class GemmReluError(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "path", "mma_m", "mma_n", "tile_m", "tile_n", "tiles_m", "tiles_n", "num_tiles",
-        "num_kb", "group_m", "grid", "cluster", "dp_tiles", "sk_tiles", "sk_q", "sk_r", "max_slots",
+        "num_kb", "group_m", "grid", "cluster", "dp_tiles", "sk_tiles", "sk_q", "sk_r", "splits", "max_slots",
         "num_stages", "stage_bytes", "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_int64), ("counter_count", ctypes.c_int64)]
 

@@ -329,10 +329,14 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
         if (!ok) return;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + buf * cols_per_buf;
-        // partial tiles are kept per CTA (one per pair half)
+        // partial tiles are kept per CTA (one per pair half), fp32, as
+        // float4 groups of 4 columns interleaved by lane:
+        //   element (col, lane) at ((col / 4) * 128 + lane) * 4 + col % 4
+        // so a warp writes / reads 512 contiguous bytes per instruction
         const int64_t split_id = T::kPair ? (int64_t)w.sk_index * 2 + rank : (int64_t)w.sk_index;
-        float* part = nullptr;
-        if (w.nslots > 1) part = p.ws + (split_id * pl.max_slots + w.slot) * tile_elems;
+        float4* part = nullptr;
+        if (w.nslots > 1)
+            part = reinterpret_cast<float4*>(p.ws + (split_id * pl.max_slots + w.slot) * tile_elems);
         for (uint32_t c = 0; c < ncols; c += T::kCols) {
             __syncwarp();  // tcgen05.ld is warp-collective
             tmem_load_chunk<kMode>(taddr + c, v);
@@ -340,7 +344,9 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
                 store_chunk<kMode>(p, w, out_row, c, v);
             } else {
 #pragma unroll
-                for (int j = 0; j < T::kCols; ++j) __stcg(part + (int64_t)(c + j) * 128 + lane_row, v[j]);
+                for (int j = 0; j < T::kCols / 4; ++j)
+                    __stcg(part + (int64_t)(c / 4 + j) * 128 + lane_row,
+                           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             }
         }
         // accumulator buffer back to the MMA warp
@@ -365,14 +371,42 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
             named_bar_sync(kEpiBarrier, kEpiThreads);
             if (*last_flag) {
                 __threadfence();
-                const float* base = p.ws + split_id * pl.max_slots * tile_elems;
+                // sum the slots in slot order; kGroup slots' loads in flight
+                constexpr int kQ = T::kCols / 4;
+                constexpr int kGroup = (T::kCols == 32) ? 2 : 4;
+                const float4* base = reinterpret_cast<const float4*>(p.ws + split_id * pl.max_slots * tile_elems);
+                const int64_t slot_q = tile_elems / 4;
                 for (uint32_t c = 0; c < ncols; c += T::kCols) {
+                    float4 acc[kQ];
 #pragma unroll
-                    for (int j = 0; j < T::kCols; ++j) v[j] = 0.0f;
-                    for (int32_t s = 0; s < w.nslots; ++s) {
-                        const float* src = base + (int64_t)s * tile_elems + (int64_t)c * 128 + lane_row;
+                    for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4* src = base + (int64_t)(c / 4) * 128 + lane_row;
+                    for (int32_t s0 = 0; s0 < w.nslots; s0 += kGroup) {
+                        float4 x[kGroup][kQ];
 #pragma unroll
-                        for (int j = 0; j < T::kCols; ++j) v[j] += __ldcg(src + (int64_t)j * 128);
+                        for (int g = 0; g < kGroup; ++g)
+                            if (s0 + g < w.nslots) {
+#pragma unroll
+                                for (int j = 0; j < kQ; ++j) x[g][j] = __ldcg(src + (s0 + g) * slot_q + j * 128);
+                            }
+#pragma unroll
+                        for (int g = 0; g < kGroup; ++g)
+                            if (s0 + g < w.nslots) {
+#pragma unroll
+                                for (int j = 0; j < kQ; ++j) {
+                                    acc[j].x += x[g][j].x;
+                                    acc[j].y += x[g][j].y;
+                                    acc[j].z += x[g][j].z;
+                                    acc[j].w += x[g][j].w;
+                                }
+                            }
+                    }
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) {
+                        v[4 * j] = acc[j].x;
+                        v[4 * j + 1] = acc[j].y;
+                        v[4 * j + 2] = acc[j].z;
+                        v[4 * j + 3] = acc[j].w;
                     }
                     store_chunk<kMode>(p, w, out_row, c, v);
                 }

@@ -94,11 +94,16 @@ static int32_t compute_max_slots(const gemm_relu_plan_t& p) {
     return best;
 }
 
-static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t sk) {
+static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t sk,
+                         int32_t splits = 1) {
     p.grid = grid;
     p.dp_tiles = dp;
     p.sk_tiles = sk;
-    if (sk > 0) {
+    p.splits = (sk > 0 && splits > 1) ? splits : 1;
+    if (sk > 0 && p.splits > 1) {
+        p.sk_q = p.sk_r = 0;
+        p.max_slots = p.splits;
+    } else if (sk > 0) {
         const int64_t units = (int64_t)sk * p.num_kb;
         p.sk_q = (int32_t)(units / grid);
         p.sk_r = (int32_t)(units % grid);
@@ -151,7 +156,7 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
 
 // Choose the best split for the current shape over at most `workers`
 // persistent workers; returns its estimated cost.
-static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only) {
+static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, int32_t force_splits) {
     const Costs c = costs_for(p.path, p.mma_n, p.stage_bytes);
     const int32_t T = p.num_tiles;
     gemm_relu_plan_t best = p;
@@ -169,6 +174,15 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only) {
             best = q;
         }
     };
+    if (force_splits > 1) {
+        // every tile cut into force_splits K ranges (at most one per k-block)
+        const int32_t sp = force_splits < p.num_kb ? force_splits : p.num_kb;
+        const int64_t items = (int64_t)T * sp;
+        gemm_relu_plan_t q = p;
+        finish_split(q, (int32_t)(items < workers ? items : workers), 0, T, sp);
+        p = q;
+        return estimate(q, c);
+    }
     // plain data-parallel
     consider(T < workers ? T : workers, T, 0);
     if (!dp_only) {
@@ -217,6 +231,12 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
 
     const char* f = force ? force : "";
     const bool dp_only = contains(f, ":dp");
+    int32_t force_splits = 0;
+    for (const char* q = f; *q; ++q)
+        if (q[0] == ':' && q[1] == 's' && q[2] >= '0' && q[2] <= '9') {
+            force_splits = 0;
+            for (const char* d = q + 2; *d >= '0' && *d <= '9'; ++d) force_splits = force_splits * 10 + (*d - '0');
+        }
     int32_t pairs = (max_pairs > 0 && max_pairs < num_sms / 2) ? max_pairs : num_sms / 2;
 
     bool want_swap = M <= 128, want_t256 = M > 128, want_t128 = M > 128, want_pair = M > 128 && pairs > 0;
@@ -239,7 +259,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         gemm_relu_plan_t q;
         memset(&q, 0, sizeof(q));
         shape_plan(q, M, N, K, path, mma_n);
-        const double cost = choose_split(q, workers, dp_only);
+        const double cost = choose_split(q, workers, dp_only, force_splits);
         if (best_cost < 0.0 || cost < best_cost) {
             best_cost = cost;
             *plan = q;

@@ -68,13 +68,16 @@ struct WorkItem {
 struct WorkIter {
     int32_t cta;
     int32_t dp_i, dp_n;
-    int64_t u, u1;
+    int64_t u, u1;  // stream-K units, or split items when p.splits > 1
 
     GR_HD void init(const gemm_relu_plan_t& p, int32_t c) {
         cta = c;
         dp_i = 0;
         dp_n = (c < p.dp_tiles) ? (p.dp_tiles - 1 - c) / p.grid + 1 : 0;
-        if (p.sk_tiles > 0) {
+        if (p.sk_tiles > 0 && p.splits > 1) {
+            u = c;
+            u1 = (int64_t)p.sk_tiles * p.splits;
+        } else if (p.sk_tiles > 0) {
             u = sk_begin(p, c);
             u1 = sk_begin(p, c + 1);
         } else {
@@ -91,6 +94,22 @@ struct WorkIter {
             w.nslots = 1;
             w.sk_index = -1;
             ++dp_i;
+            tile_coords(p, w.tile, w.tm, w.tn);
+            return true;
+        }
+        if (p.splits > 1) {
+            if (u >= u1) return false;
+            // split item: tile fastest, so workers running together read
+            // the same K range of neighbouring tiles
+            const int32_t t = (int32_t)(u % p.sk_tiles);
+            const int32_t sp = (int32_t)(u / p.sk_tiles);
+            w.sk_index = t;
+            w.tile = p.dp_tiles + t;
+            w.kb0 = (int32_t)((int64_t)sp * p.num_kb / p.splits);
+            w.kb1 = (int32_t)((int64_t)(sp + 1) * p.num_kb / p.splits);
+            w.slot = sp;
+            w.nslots = p.splits;
+            u += p.grid;
             tile_coords(p, w.tile, w.tm, w.tn);
             return true;
         }
