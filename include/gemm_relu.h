@@ -36,7 +36,8 @@ typedef enum {
     GEMM_ERR_OUT_OF_MEMORY = 4,      /* library-owned workspace could not be allocated */
     GEMM_ERR_LAUNCH = 5,             /* the kernel launch failed */
     GEMM_ERR_TIMEOUT = 6,            /* a device-side wait exceeded its limit (reported later) */
-    GEMM_ERR_CUDA = 7                /* another CUDA runtime error */
+    GEMM_ERR_CUDA = 7,               /* another CUDA runtime error */
+    GEMM_ERR_TOO_LARGE = 8           /* gemm_relu_noalloc: problem outside its fixed scratch */
 } gemm_status_t;
 
 /* Largest accepted M, N or K (TMA coordinates are signed 32-bit). */
@@ -90,6 +91,47 @@ const char* gemm_relu_status_string(int status);
 /* Frees every library-owned device buffer on every device.  Must not be
  * called while work of this library is in flight. */
 void gemm_relu_shutdown(void);
+
+/* ---- Entry point that allocates nothing -------------------------------- */
+
+/* Bytes of the fixed device scratch array behind gemm_relu_noalloc (one per
+ * device that loads the library, held until the process exits). */
+#define GEMM_RELU_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * Same operation and arguments as gemm_relu, for callers that must not
+ * allocate device memory.  gemm_relu grows a split-K workspace with
+ * cudaMalloc the first time a shape needs one, and cudaMalloc / cudaFree
+ * can synchronize the device; a caller in a loop that must never stall on
+ * an allocation, or a process whose device memory is entirely reserved by
+ * another allocator, cannot allow that.  This entry point never calls
+ * cudaMalloc, cudaFree or any allocating routine: it runs the small-M
+ * (swapped-operand) kernel with its split-K partial tiles, arrival
+ * counters and error word in a fixed array of
+ * GEMM_RELU_NOALLOC_SCRATCH_BYTES in device memory.  The caller still owns
+ * and passes A, B and C (device pointers, same layout and alignment rules
+ * as gemm_relu).  There is no counterpart on the pages: it is a deployment
+ * convenience.
+ *
+ * Limits: 1 <= M <= 128 and K >= 1, and the split-K partials of the chosen
+ * plan must fit in the array (about 8 MiB: ceil(N / 128) x round_up(M, 16)
+ * x 512 bytes x the number of CTAs sharing a tile); otherwise it returns
+ * GEMM_ERR_TOO_LARGE without launching anything.  M == 0 or N == 0 is a
+ * no-op.
+ *
+ * The first call on a device does a one-time set-up there (device check,
+ * the scratch array's device address via cudaGetSymbolAddress, kernel
+ * attributes); make that first call before any stream capture.  Every call
+ * on a device shares the one array and finds it as the previous call left
+ * it: each call first clears, on `stream`, the counters and error word it
+ * needs to start at zero.  Calls whose execution overlaps on the GPU (e.g.
+ * on two streams) race on the array and give undefined results; issue them
+ * in one stream or otherwise ordered.  A timed-out device wait in this
+ * variant is recorded in the array's error word, not in the word that
+ * gemm_relu_check_device_error reads.
+ */
+int gemm_relu_noalloc(const void* A, const void* B, void* C,
+                      int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);
 
 /* ---- Host-only planning interface (no CUDA calls; usable without a GPU) -- */
 

@@ -18,7 +18,7 @@ GEMM_OK = 0
 STATUS_NAMES = {
     0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_ALIGNMENT",
     3: "GEMM_ERR_UNSUPPORTED_DEVICE", 4: "GEMM_ERR_OUT_OF_MEMORY", 5: "GEMM_ERR_LAUNCH",
-    6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_CUDA",
+    6: "GEMM_ERR_TIMEOUT", 7: "GEMM_ERR_CUDA", 8: "GEMM_ERR_TOO_LARGE",
 }
 
 
@@ -67,6 +67,8 @@ def lib():
         L.gemm_relu.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
         L.gemm_relu_host.restype = i32
         L.gemm_relu_host.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_noalloc.restype = i32
+        L.gemm_relu_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
         L.gemm_relu_check_device_error.restype = i32
         L.gemm_relu_check_device_error.argtypes = [vp]
         L.gemm_relu_status_string.restype = ctypes.c_char_p

@@ -498,10 +498,4 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-__global__ void zero_fill_kernel(uint4* c, int64_t n16) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
-        c[i] = make_uint4(0u, 0u, 0u, 0u);
-}
-
 }  // namespace gr

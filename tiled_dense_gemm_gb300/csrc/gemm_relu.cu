@@ -15,6 +15,14 @@
 #include "gemm_relu.h"
 
 namespace gr {
+
+// C := +0 for K == 0 (the empty sum).
+__global__ void zero_fill_kernel(uint4* c, int64_t n16) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        c[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -385,6 +393,7 @@ extern "C" const char* gemm_relu_status_string(int status) {
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE";
         default: return "GEMM_ERR_UNKNOWN";
     }
 }
