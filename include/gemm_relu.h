@@ -159,7 +159,8 @@ typedef struct {
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
-    int64_t counter_count;   /* arrival counters (one per stream-K tile and CTA of a worker) */
+    int64_t counter_count;   /* arrival counters (one per split tile and CTA of a worker); the
+                                counter array also holds max_slots ready flags per counter */
 } gemm_relu_plan_t;
 
 /*
@@ -168,7 +169,8 @@ typedef struct {
  * num_sms / 2; the runtime also caps them by the device's co-resident
  * cluster count).  Pure host code.  The environment variable
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
- * "tiled256", "tiled128", "swap" (M <= 128 only) or "pair", optionally
+ * "tiled256", "tiled128", "swap" (M <= 128 only), "swapnW" (M <= 128,
+ * data-parallel tiles W = 8..64 columns wide) or "pair", optionally
  * followed by ":dp" to forbid splitting tiles along K, or by ":sN" to cut
  * every tile into N equal K ranges (the split schedule).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.

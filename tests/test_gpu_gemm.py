@@ -258,14 +258,16 @@ def test_stream_k_counters_are_left_zero():
 # ---------------------------------------------------------------- every kernel shape
 
 FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (1024, 1024, 1024),
-                 (257, 1032, 4104), (96, 2048, 3000)]
+                 (257, 1032, 4104), (96, 2048, 3000), (48, 6144, 2048), (8, 4864, 1024)]
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "tiled128:dp",
-                                   "pair:dp", "swap", "swap:dp", "swap:s7", "tiled128:s3", "pair:s5"])
+                                   "pair:dp", "swap", "swap:dp", "swap:s7", "swapn56", "swapn8",
+                                   "tiled128:s3", "pair:s5"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
-    swapped operands), with and without stream-K splitting, on ragged shapes."""
+    swapped operands with 128-wide or narrow tiles), with and without
+    stream-K / split-K, on ragged shapes."""
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     for M, N, K in FORCED_SHAPES:
         A, B = make_inputs(M, N, K, seed=M + N + K, dist_a="uniform", dist_b="uniform")

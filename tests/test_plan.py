@@ -17,7 +17,8 @@ SMEM_LIMIT = 227 * 1024
 SHAPES = [(w.M, w.N, w.K) for w in WORKLOADS.values()] + [
     (1, 8, 8), (8, 8, 8), (127, 8, 64), (129, 136, 72), (257, 264, 2056), (128, 128, 128),
     (256, 512, 64), (4096, 8192, 64), (64, 4096, 16384), (1000, 1000, 8), (2048, 2048, 2048),
-    (8192, 8192, 8192), (130, 24, 4104), (16, 65536, 512), (100000, 8, 8),
+    (8192, 8192, 8192), (130, 24, 4104), (16, 65536, 512), (100000, 8, 8), (48, 6144, 2048),
+    (8, 4864, 1024),
 ]
 
 
@@ -31,7 +32,8 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     else:
         assert d["path"] in (2, 4)
     if d["path"] == 3:
-        assert d["mma_n"] == ((M + 15) // 16) * 16 and d["tile_n"] == 128
+        assert d["mma_n"] == ((M + 15) // 16) * 16
+        assert d["tile_n"] == 128 or (8 <= d["tile_n"] <= 64 and d["tile_n"] % 8 == 0 and d["sk_tiles"] == 0)
         assert d["mma_m"] == 128 and d["cluster"] == 1
     elif d["path"] == 2:
         assert d["mma_n"] in (128, 256) and d["tile_m"] == 128
@@ -103,7 +105,8 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
-                                   "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3"])
+                                   "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3", "swapn56",
+                                   "swapn8"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256)}
@@ -144,4 +147,4 @@ def test_headline_shapes_use_the_intended_kernels(gemm_lib):
     sq = gemm_lib.plan(4096, 4096, 4096, 152)
     assert sq.path == 4 and sq.grid == 76 and sq.cluster == 2
     sk = gemm_lib.plan(16, 8192, 8192, 152)
-    assert sk.path == 3 and sk.mma_n == 16 and sk.grid == 152 and sk.sk_tiles == sk.num_tiles
+    assert sk.path == 3 and sk.mma_n == 16 and sk.tile_n == 128

@@ -68,11 +68,11 @@ def test_noalloc_rejects_what_its_scratch_cannot_hold():
     c = torch.zeros(129, 64, dtype=torch.float16, device=DEV)
     assert call_noalloc(a, b, c) == 8  # GEMM_ERR_TOO_LARGE: M > 128
     assert binding.status_string(8) == "GEMM_ERR_TOO_LARGE"
-    # M = 128, N = 4096, K = 1024: its split-K partials need 8 MiB, more
-    # than the array holds beside its counters
-    a2 = torch.zeros(128, 1024, dtype=torch.float16, device=DEV)
-    b2 = torch.zeros(1024, 4096, dtype=torch.float16, device=DEV)
-    c2 = torch.zeros(128, 4096, dtype=torch.float16, device=DEV)
+    # M = 128, N = 2048, K = 16384: its split-K partials need 11 MiB, more
+    # than the array holds
+    a2 = torch.zeros(128, 16384, dtype=torch.float16, device=DEV)
+    b2 = torch.zeros(16384, 2048, dtype=torch.float16, device=DEV)
+    c2 = torch.zeros(128, 2048, dtype=torch.float16, device=DEV)
     assert call_noalloc(a2, b2, c2) == 8
     base = torch.zeros(16 * 64 + 1, dtype=torch.float16, device=DEV)
     assert call_noalloc(base[1:].view(16, 64), b, c[:16]) == 2  # misaligned A

@@ -87,7 +87,6 @@ struct ModeTraits {
     static constexpr uint32_t kBN = (kMode == 1) ? 128 : 256;  // C columns per tile (normal)
     static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
     static constexpr uint32_t kBCols = kPair ? 128 : kBN;      // B columns loaded per CTA
-    static constexpr int kCols = kSwap ? 16 : 32;              // TMEM columns per epilogue load
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
@@ -140,7 +139,7 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 
 template <int kMode>
 __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
-                                              uint32_t stride, const CUtensorMap* tmA,
+                                              uint32_t stride, uint32_t a_bytes, const CUtensorMap* tmA,
                                               const CUtensorMap* tmB, int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t pl = p.plan;
@@ -152,6 +151,7 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
     // the bytes of both CTAs
     const uint32_t tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
     const int32_t tile_m = pl.tile_m;
+    const int32_t tile_n = pl.tile_n;
     WorkIter wi;
     wi.init(pl, worker);
     WorkItem w;
@@ -167,13 +167,13 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
             b_col = w.tn * (int32_t)T::kBN;
         } else {
             a_row = w.tm * tile_m;
-            b_col = w.tn * 128;
+            b_col = w.tn * tile_n;
         }
         for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
             if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return;
             const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
-            const uint32_t b_dst = a_dst + kOperandA;
+            const uint32_t b_dst = a_dst + a_bytes;
             const int32_t k0 = kb * kBlockK;
             if constexpr (T::kPair) {
                 const uint32_t full_leader = mapa_shared(full, 0);
@@ -190,9 +190,11 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
                     for (uint32_t j = 0; j < T::kBN / 64; ++j)
                         tma_load_2d(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0);
                 } else {
-                    // MMA A operand: 128 columns of B (two 64-wide chunks)
+                    // MMA A operand: the tile's columns of B, one 64-wide chunk
+                    // per TMA box (a narrow tile fills part of one chunk; the
+                    // accumulator lanes past tile_n are never stored)
                     tma_load_2d(a_dst, tmB, full, b_col, k0);
-                    tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
+                    if (tile_n > 64) tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
                     // MMA B operand: the (padded) rows of A
                     tma_load_2d(b_dst, tmA, full, k0, a_row);
                 }
@@ -207,7 +209,8 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
 
 template <int kMode>
 __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
-                                         uint32_t stride, uint32_t tmem_base, int32_t worker) {
+                                         uint32_t stride, uint32_t a_bytes, uint32_t tmem_base,
+                                         int32_t worker) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
@@ -222,8 +225,8 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     // row.  MN-major operand (B; B^T when swapped): +16 k-rows = 2 atoms.
     const uint64_t a_desc0 = T::kSwap ? make_sw128_desc(stages, kChunkBytes, kAtomBytes)
                                       : make_sw128_desc(stages, 16, kAtomBytes);
-    const uint64_t b_desc0 = T::kSwap ? make_sw128_desc(stages + kOperandA, 16, kAtomBytes)
-                                      : make_sw128_desc(stages + kOperandA, kChunkBytes, kAtomBytes);
+    const uint64_t b_desc0 = T::kSwap ? make_sw128_desc(stages + a_bytes, 16, kAtomBytes)
+                                      : make_sw128_desc(stages + a_bytes, kChunkBytes, kAtomBytes);
     constexpr uint32_t kAStep = (T::kSwap ? 2 * kAtomBytes : 32u) >> 4;
     constexpr uint32_t kBStep = (T::kSwap ? 32u : 2 * kAtomBytes) >> 4;
     const uint32_t stride16 = stride >> 4;
@@ -259,176 +262,272 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     }
 }
 
-// Store one epilogue chunk (kCols accumulator columns of this thread's
-// TMEM lane) to C.
+// ------------------------------------------------------------------ epilogue
+//
+// The epilogue works on chunks of kChunk accumulator columns of its TMEM
+// lane (= one output row for the tiled paths, one output column for the
+// swapped path):
+//   tiled / pair: 64 columns.  ReLU + round to fp16, written by each warp
+//     into its own 128B-swizzled 32-row x 128-byte staging buffer (two per
+//     warp, alternating), then stored by one TMA bulk copy per warp; the
+//     copy clips rows >= M and columns >= N.
+//   swapped: 16 columns (16 rows of C).  Stored directly: a warp writes 32
+//     consecutive elements of one C row per instruction.
+
 template <int kMode>
-__device__ __forceinline__ void store_chunk(const KParams& p, const WorkItem& w, uint32_t lane_row,
-                                            uint32_t col0, const float* v) {
-    using T = ModeTraits<kMode>;
-    if constexpr (!T::kSwap) {
-        const int64_t m = (int64_t)w.tm * T::kTileM + lane_row;  // lane_row includes the pair half
-        if (m >= p.M) return;
-        const int64_t n0 = (int64_t)w.tn * T::kBN + col0;
-        __half* dst = p.C + m * p.N + n0;
+struct EpiTraits {
+    static constexpr int kChunk = ModeTraits<kMode>::kSwap ? 16 : 64;
+};
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 q) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(q.x), "r"(q.y), "r"(q.z),
+                 "r"(q.w)
+                 : "memory");
+}
+
+// Tiled / pair paths: one 64-column chunk of this warp's 32 rows -> C.
+// `lane` is the row within the warp's slab; `sbuf` alternates buffers.
+__device__ __forceinline__ void sink_tma(const CUtensorMap* tmC, uint32_t stage_buf, uint32_t lane,
+                                         const float* v, int32_t apply_relu, int64_t col, int64_t row0,
+                                         int64_t M, int64_t N) {
+    // the copy issued two chunks ago from this buffer must have read it
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row_addr = stage_buf + lane * 128u;
 #pragma unroll
-        for (int g = 0; g < T::kCols / 8; ++g) {
-            if (n0 + 8 * g < p.N) {  // N % 8 == 0: an 8-column group is all in or all out
-                uint4 q;
-                q.x = pack_half2(relu_if(v[8 * g + 0], p.apply_relu), relu_if(v[8 * g + 1], p.apply_relu));
-                q.y = pack_half2(relu_if(v[8 * g + 2], p.apply_relu), relu_if(v[8 * g + 3], p.apply_relu));
-                q.z = pack_half2(relu_if(v[8 * g + 4], p.apply_relu), relu_if(v[8 * g + 5], p.apply_relu));
-                q.w = pack_half2(relu_if(v[8 * g + 6], p.apply_relu), relu_if(v[8 * g + 7], p.apply_relu));
-                *reinterpret_cast<uint4*>(dst + 8 * g) = q;
-            }
-        }
-    } else {
-        const int64_t n = (int64_t)w.tn * 128 + lane_row;
-        if (n >= p.N) return;
-        const int64_t m0 = (int64_t)w.tm * p.plan.tile_m + col0;
-#pragma unroll
-        for (int j = 0; j < T::kCols; ++j) {
-            const int64_t m = m0 + j;
-            if (m < p.M) p.C[m * p.N + n] = __float2half_rn(relu_if(v[j], p.apply_relu));
-        }
+    for (uint32_t u = 0; u < 8; ++u) {
+        uint4 q;
+        q.x = pack_half2(relu_if(v[8 * u + 0], apply_relu), relu_if(v[8 * u + 1], apply_relu));
+        q.y = pack_half2(relu_if(v[8 * u + 2], apply_relu), relu_if(v[8 * u + 3], apply_relu));
+        q.z = pack_half2(relu_if(v[8 * u + 4], apply_relu), relu_if(v[8 * u + 5], apply_relu));
+        q.w = pack_half2(relu_if(v[8 * u + 6], apply_relu), relu_if(v[8 * u + 7], apply_relu));
+        st_shared_v4(row_addr + ((u ^ (lane & 7u)) << 4), q);  // 128-byte swizzle
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (col < N && row0 < M) tma_store_2d(tmC, stage_buf, (int32_t)col, (int32_t)row0);
+        bulk_commit_group();
+    }
+}
+
+// Swapped path: 16 accumulator columns (= C rows m0 .. m0+15) of C column n.
+__device__ __forceinline__ void sink_direct_swap(__half* C, const float* v, int32_t apply_relu,
+                                                 int64_t n, int64_t m0, int64_t M, int64_t N) {
+    if (n >= N) return;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (m0 + j < M) C[(m0 + j) * N + n] = __float2half_rn(relu_if(v[j], apply_relu));
 }
 
 template <int kMode>
 __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
-    using T = ModeTraits<kMode>;
-    if constexpr (T::kCols == 32) {
+    if constexpr (EpiTraits<kMode>::kChunk == 64) {
         tmem_load_32cols(taddr, *reinterpret_cast<float(*)[32]>(v));
+        tmem_load_32cols(taddr + 32, *reinterpret_cast<float(*)[32]>(v + 32));
     } else {
         tmem_load_16cols(taddr, *reinterpret_cast<float(*)[16]>(v));
     }
 }
 
 template <int kMode>
-__device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base, int32_t worker) {
+__device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base,
+                                              int32_t worker, const CUtensorMap* tmC,
+                                              uint32_t staging) {
     using T = ModeTraits<kMode>;
-    const gemm_relu_plan_t& pl = p.plan;
+    constexpr int kChunk = EpiTraits<kMode>::kChunk;
+    constexpr int kQ = kChunk / 4;  // float4 groups per chunk
+    const gemm_relu_plan_t pl = p.plan;
+    const int64_t M = p.M, N = p.N;
+    const int32_t apply_relu = p.apply_relu;
+    __half* const C = p.C;
+    float* const ws = p.ws;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
     const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
-    const uint32_t lane_row = quarter * 32 + lane;             // TMEM lane = accumulator row
-    const uint32_t out_row = lane_row + 128u * rank;           // row within the C tile
+    const uint32_t lane_row = quarter * 32 + lane;  // TMEM lane = accumulator row
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
     const int64_t tile_elems = (int64_t)128 * ncols;
+    const uint32_t my_staging = staging + quarter * 8192u;  // two 4 KiB buffers per warp
+    uint32_t sbuf = 0;
     volatile int32_t* last_flag = &ctrl->last_flag;
     WorkIter wi;
     wi.init(pl, worker);
     WorkItem w;
     uint32_t local = 0;
-    float v[T::kCols];
+    float v[kChunk];
+
+    // where chunk c of this thread's lane goes
+    auto sink = [&](const WorkItem& it, uint32_t c) {
+        if constexpr (T::kSwap) {
+            if (lane_row < (uint32_t)pl.tile_n)
+                sink_direct_swap(C, v, apply_relu, (int64_t)it.tn * pl.tile_n + lane_row,
+                                 (int64_t)it.tm * pl.tile_m + c, M, N);
+        } else {
+            const int64_t row0 = (int64_t)it.tm * T::kTileM + 128 * rank + 32 * quarter;
+            const int64_t col = (int64_t)it.tn * T::kBN + c;
+            sink_tma(tmC, my_staging + sbuf * 4096u, lane, v, apply_relu, col, row0, M, N);
+            sbuf ^= 1u;
+        }
+    };
+
     while (wi.next(pl, w)) {
         const uint32_t buf = local & 1u;
         const uint32_t bph = (local >> 1) & 1u;
         bool ok = wait_phase(smem_u32(&ctrl->tmem_full[buf]), bph, ctrl, p, kErrEpilogue);
         ok = named_bar_and(kEpiBarrier, kEpiThreads, ok);  // all epilogue warps agree
-        if (!ok) return;
+        if (!ok) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((quarter * 32u) << 16) + buf * cols_per_buf;
-        // partial tiles are kept per CTA (one per pair half), fp32, as
-        // float4 groups of 4 columns interleaved by lane:
+        // accumulator buffer back to the MMA warp
+        auto release_tmem = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (T::kPair)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->tmem_empty[buf]), 0));
+                else
+                    mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
+            }
+        };
+        if (w.nslots == 1) {
+            for (uint32_t c = 0; c < ncols; c += kChunk) {
+                __syncwarp();  // tcgen05.ld is warp-collective
+                tmem_load_chunk<kMode>(taddr + c, v);
+                sink(w, c);
+            }
+            release_tmem();
+            ++local;
+            continue;
+        }
+        // A tile split along K (one share per slot).  Each CTA first takes
+        // an arrival ticket.  All but the last write their fp32 partial and
+        // then raise their slot's ready flag; the last waits for the other
+        // slots' flags and sums the slots in slot order, its own share read
+        // straight from tensor memory, so its partial is never written.
+        // Partials are per CTA (one per pair half), as float4 groups of 4
+        // columns interleaved by lane:
         //   element (col, lane) at ((col / 4) * 128 + lane) * 4 + col % 4
-        // so a warp writes / reads 512 contiguous bytes per instruction
+        // so a warp writes / reads 512 contiguous bytes per instruction.
         const int64_t split_id = T::kPair ? (int64_t)w.sk_index * 2 + rank : (int64_t)w.sk_index;
-        float4* part = nullptr;
-        if (w.nslots > 1)
-            part = reinterpret_cast<float4*>(p.ws + (split_id * pl.max_slots + w.slot) * tile_elems);
-        for (uint32_t c = 0; c < ncols; c += T::kCols) {
-            __syncwarp();  // tcgen05.ld is warp-collective
-            tmem_load_chunk<kMode>(taddr + c, v);
-            if (w.nslots == 1) {
-                store_chunk<kMode>(p, w, out_row, c, v);
-            } else {
+        uint32_t* const counter = p.counters + split_id;
+        uint32_t* const flags = p.counters + pl.counter_count + split_id * pl.max_slots;
+        named_bar_sync(kEpiBarrier, kEpiThreads);  // last_flag of the previous item is consumed
+        if (threadIdx.x == 64) {
+            const uint32_t prev = atomicAdd(counter, 1u);
+            *last_flag = (prev == (uint32_t)(w.nslots - 1)) ? 1 : 0;
+        }
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        const bool last = *last_flag != 0;
+        const float4* const base = reinterpret_cast<const float4*>(ws + split_id * pl.max_slots * tile_elems);
+        const int64_t slot_q = tile_elems / 4;
+        if (!last) {
+            float4* part = const_cast<float4*>(base) + w.slot * slot_q;
+            for (uint32_t c = 0; c < ncols; c += kChunk) {
+                __syncwarp();
+                tmem_load_chunk<kMode>(taddr + c, v);
 #pragma unroll
-                for (int j = 0; j < T::kCols / 4; ++j)
+                for (int j = 0; j < kQ; ++j)
                     __stcg(part + (int64_t)(c / 4 + j) * 128 + lane_row,
                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             }
-        }
-        // accumulator buffer back to the MMA warp
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-            if constexpr (T::kPair)
-                mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->tmem_empty[buf]), 0));
-            else
-                mbar_arrive(smem_u32(&ctrl->tmem_empty[buf]));
-        }
-        if (w.nslots > 1) {
-            // publish the partial, count arrivals; the last CTA reduces
-            __threadfence();
+            release_tmem();
+            __threadfence();  // the partial is visible before the flag
             named_bar_sync(kEpiBarrier, kEpiThreads);
-            if (threadIdx.x == 64) {
-                const uint32_t prev = atomicAdd(&p.counters[split_id], 1u);
-                const int32_t last = (prev == (uint32_t)(w.nslots - 1)) ? 1 : 0;
-                if (last) p.counters[split_id] = 0u;  // ready for the next launch
-                *last_flag = last;
-            }
-            named_bar_sync(kEpiBarrier, kEpiThreads);
-            if (*last_flag) {
-                __threadfence();
-                // sum the slots in slot order; kGroup slots' loads in flight
-                constexpr int kQ = T::kCols / 4;
-                constexpr int kGroup = (T::kCols == 32) ? 2 : 4;
-                const float4* base = reinterpret_cast<const float4*>(p.ws + split_id * pl.max_slots * tile_elems);
-                const int64_t slot_q = tile_elems / 4;
-                for (uint32_t c = 0; c < ncols; c += T::kCols) {
-                    float4 acc[kQ];
-#pragma unroll
-                    for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4* src = base + (int64_t)(c / 4) * 128 + lane_row;
-                    for (int32_t s0 = 0; s0 < w.nslots; s0 += kGroup) {
-                        float4 x[kGroup][kQ];
-#pragma unroll
-                        for (int g = 0; g < kGroup; ++g)
-                            if (s0 + g < w.nslots) {
-#pragma unroll
-                                for (int j = 0; j < kQ; ++j) x[g][j] = __ldcg(src + (s0 + g) * slot_q + j * 128);
-                            }
-#pragma unroll
-                        for (int g = 0; g < kGroup; ++g)
-                            if (s0 + g < w.nslots) {
-#pragma unroll
-                                for (int j = 0; j < kQ; ++j) {
-                                    acc[j].x += x[g][j].x;
-                                    acc[j].y += x[g][j].y;
-                                    acc[j].z += x[g][j].z;
-                                    acc[j].w += x[g][j].w;
-                                }
-                            }
+            if (threadIdx.x == 64) atomicExch(flags + w.slot, 1u);
+            ++local;
+            continue;
+        }
+        // last arriver: every other slot has taken its ticket; wait (bounded)
+        // until each has published its partial
+        bool ready = true;
+        if (threadIdx.x == 64) {
+            volatile uint32_t* vf = flags;
+            volatile int32_t* abort_flag = &ctrl->abort_flag;
+            const uint64_t t0 = globaltimer_ns();
+            for (int32_t sl = 0; sl < w.nslots && ready; ++sl) {
+                if (sl == w.slot) continue;
+                while (vf[sl] == 0u) {
+                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                        *abort_flag = 1;
+                        atomicCAS(p.err, 0, kErrEpilogue);
+                        ready = false;
+                        break;
                     }
-#pragma unroll
-                    for (int j = 0; j < kQ; ++j) {
-                        v[4 * j] = acc[j].x;
-                        v[4 * j + 1] = acc[j].y;
-                        v[4 * j + 2] = acc[j].z;
-                        v[4 * j + 3] = acc[j].w;
-                    }
-                    store_chunk<kMode>(p, w, out_row, c, v);
                 }
             }
         }
+        ready = named_bar_and(kEpiBarrier, kEpiThreads, ready);
+        if (!ready) {
+            release_tmem();
+            break;
+        }
+        __threadfence();
+        for (uint32_t c = 0; c < ncols; c += kChunk) {
+            __syncwarp();
+            tmem_load_chunk<kMode>(taddr + c, v);  // own share
+            float4 acc[kQ];
+#pragma unroll
+            for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4* src = base + (int64_t)(c / 4) * 128 + lane_row;
+            for (int32_t sl = 0; sl < w.nslots; ++sl) {
+                float4 x[kQ];
+                if (sl == w.slot) {
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) x[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) x[j] = __ldcg(src + sl * slot_q + j * 128);
+                }
+#pragma unroll
+                for (int j = 0; j < kQ; ++j) {
+                    acc[j].x += x[j].x;
+                    acc[j].y += x[j].y;
+                    acc[j].z += x[j].z;
+                    acc[j].w += x[j].w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kQ; ++j) {
+                v[4 * j] = acc[j].x;
+                v[4 * j + 1] = acc[j].y;
+                v[4 * j + 2] = acc[j].z;
+                v[4 * j + 3] = acc[j].w;
+            }
+            sink(w, c);
+        }
+        release_tmem();
+        named_bar_sync(kEpiBarrier, kEpiThreads);
+        if (threadIdx.x == 64) {
+            // every slot of this tile has arrived and published: reset the
+            // counter and flags for the next launch
+            for (int32_t sl = 0; sl < w.nslots; ++sl) flags[sl] = 0u;
+            *counter = 0u;
+        }
         ++local;
     }
+    // every TMA store of C issued by this warp has completed
+    if (!T::kSwap && lane == 0) bulk_wait_group_all();
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ KParams p) {
+    gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
     using T = ModeTraits<kMode>;
     extern __shared__ __align__(1024) uint8_t smem[];
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
     const uint32_t base = smem_u32(smem);
     const uint32_t stages = (base + (uint32_t)sizeof(Ctrl) + 1023u) & ~1023u;
     const gemm_relu_plan_t& pl = p.plan;
-    const uint32_t a_bytes = kOperandA;
+    // MMA A operand per stage: two 64-wide chunks, or one for a narrow
+    // swapped tile (its second chunk then reads the next bytes of shared
+    // memory; those accumulator lanes are never stored)
+    const uint32_t a_bytes = (T::kSwap && pl.tile_n <= 64) ? kChunkBytes : kOperandA;
     const uint32_t b_bytes = (T::kPair ? T::kBCols * kBlockK * 2
                                        : ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
@@ -439,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (!T::kSwap) tma_prefetch_desc(&tmC);
         for (int s = 0; s < pl.num_stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
             mbar_init(smem_u32(&ctrl->empty[s]), 1);
@@ -466,18 +566,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = ctrl->tmem_addr;
 
     if (warp == 0) {
-        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, &tmA, &tmB, worker);
+        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, worker);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {  // one thread of the (leader) CTA issues every MMA
-            mma_role<kMode>(p, ctrl, stages, stride, tmem_base, worker);
+            mma_role<kMode>(p, ctrl, stages, stride, a_bytes, tmem_base, worker);
             // no MMA may still be running when tensor memory is released
             mma_commit<T::kCG>(smem_u32(&ctrl->final_bar), 0x1);
             if (!wait_phase_for(smem_u32(&ctrl->final_bar), 0, p.timeout_ns)) atomicCAS(p.err, 0, kErrFinal);
         }
         __syncwarp();
     } else {
-        epilogue_role<kMode>(p, ctrl, tmem_base, worker);
+        // C staging for the TMA stores sits after the ring (tiled paths)
+        const uint32_t staging = stages + (uint32_t)pl.num_stages * stride;
+        epilogue_role<kMode>(p, ctrl, tmem_base, worker, &tmC, staging);
     }
 
     if (warp == 0 && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {

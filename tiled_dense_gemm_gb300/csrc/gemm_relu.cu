@@ -32,8 +32,8 @@ struct StreamBuffers {
     void* stream = nullptr;
     float* ws = nullptr;  // stream-K partial tiles
     size_t ws_bytes = 0;
-    uint32_t* counters = nullptr;  // stream-K arrival counters (kept zero between launches)
-    size_t n_counters = 0;
+    uint32_t* counters = nullptr;  // split-K arrival counters + ready flags (zero between launches)
+    size_t counter_bytes = 0;
     void* hA = nullptr;  // staging for the host-buffer entry point
     void* hB = nullptr;
     void* hC = nullptr;
@@ -189,7 +189,7 @@ int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
 
 template <int kMode>
 int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, const CUtensorMap& ta,
-                const CUtensorMap& tb, cudaStream_t st) {
+                const CUtensorMap& tb, const CUtensorMap& tc, cudaStream_t st) {
     auto fn = gemm_relu_kernel<kMode>;
     if (!d.attr_set[kMode]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) !=
@@ -213,7 +213,7 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, kp) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, kp) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -282,8 +282,9 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         StreamBuffers& sb = buffers_for_locked(d, st);
         int rc = grow(reinterpret_cast<void**>(&sb.ws), &sb.ws_bytes, (size_t)pl.workspace_bytes, st, false);
         if (rc != GEMM_OK) return rc;
-        rc = grow(reinterpret_cast<void**>(&sb.counters), &sb.n_counters,
-                  (size_t)pl.counter_count * sizeof(uint32_t), st, true);
+        // one arrival counter per split tile, then max_slots ready flags each
+        rc = grow(reinterpret_cast<void**>(&sb.counters), &sb.counter_bytes,
+                  (size_t)pl.counter_count * (1 + (size_t)pl.max_slots) * sizeof(uint32_t), st, true);
         if (rc != GEMM_OK) return rc;
         kp.ws = sb.ws;
         kp.counters = sb.counters;
@@ -292,16 +293,22 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     const bool swap = (pl.path == 3);
     int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u);
     if (rc != GEMM_OK) return rc;
-    rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K, 64, kBlockK);
+    // B: 64-column boxes (a narrow swapped tile: one box of tile_n columns)
+    rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
+                   (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, kBlockK);
+    if (rc != GEMM_OK) return rc;
+    // C: 64-column x 32-row boxes, one per epilogue warp and chunk
+    CUtensorMap tc;
+    rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32);
     if (rc != GEMM_OK) return rc;
     if (swap) {
         kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
-        return launch_mode<2>(d, pl, kp, ta, tb, st);
+        return launch_mode<2>(d, pl, kp, ta, tb, tc, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);
-    if (pl.path == 4) return launch_mode<3>(d, pl, kp, ta, tb, st);
-    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, st);
-    return launch_mode<1>(d, pl, kp, ta, tb, st);
+    if (pl.path == 4) return launch_mode<3>(d, pl, kp, ta, tb, tc, st);
+    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tc, st);
+    return launch_mode<1>(d, pl, kp, ta, tb, tc, st);
 }
 
 }  // namespace
@@ -377,7 +384,7 @@ extern "C" int gemm_relu_check_device_error(void* stream) {
     cudaDeviceSynchronize();
     cudaMemset(d.d_err, 0, 16);
     for (auto& s : d.streams)
-        if (s.counters) cudaMemset(s.counters, 0, s.n_counters);
+        if (s.counters) cudaMemset(s.counters, 0, s.counter_bytes);
     cudaDeviceSynchronize();
     cudaGetLastError();
     return GEMM_ERR_TIMEOUT;

@@ -26,7 +26,8 @@ namespace {
 
 // Scratch layout (bytes):
 //   [0, 16)                error word of the kernel (int32 at 0)
-//   [256, 256 + 4 * n)     split-K arrival counters, one per split tile
+//   [256, kPartialOffset)  split-K arrival counters (one per split tile),
+//                          then max_slots ready flags per split tile
 //   [kPartialOffset, end)  fp32 partial tiles
 constexpr size_t kScratchBytes = GEMM_RELU_NOALLOC_SCRATCH_BYTES;
 constexpr size_t kCounterOffset = 256;
@@ -140,7 +141,8 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     if (rc != GEMM_OK) return rc;
     if (pl.path != 3) return GEMM_ERR_TOO_LARGE;
     const size_t partial_bytes = (size_t)pl.workspace_bytes;
-    if ((size_t)pl.counter_count > kMaxCounters || partial_bytes > kScratchBytes - kPartialOffset)
+    if ((size_t)pl.counter_count * (1 + (size_t)pl.max_slots) > kMaxCounters ||
+        partial_bytes > kScratchBytes - kPartialOffset)
         return GEMM_ERR_TOO_LARGE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -165,11 +167,14 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
     kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tc;
     if ((rc = encode(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, (uint32_t)pl.tile_m)) != GEMM_OK) return rc;
-    if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, 64, kBlockK)) != GEMM_OK) return rc;
+    if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 64u,
+                     kBlockK)) != GEMM_OK)
+        return rc;
+    if ((rc = encode(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32)) != GEMM_OK) return rc;  // unused by this kernel
 
-    gemm_relu_kernel<2><<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, kp);
+    gemm_relu_kernel<2><<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, tc, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }

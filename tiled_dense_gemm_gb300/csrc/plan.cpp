@@ -13,7 +13,9 @@ namespace gr {
 // Shared-memory layout constants (must match the kernel).
 constexpr int32_t kCtrlBytes = 1024;        // barriers + flags
 constexpr int32_t kAlignSlack = 1024;       // dynamic smem rounded up to 1 KiB
-constexpr int32_t kStageBudget = 200 * 1024;
+constexpr int32_t kSmemLimit = 227 * 1024;  // opt-in shared memory per CTA
+constexpr int32_t kStagingBytes = 32 * 1024;  // C staging for TMA stores (tiled paths)
+constexpr int32_t kSwapStageBudget = 200 * 1024;
 constexpr int32_t kMaxStages = 16;
 constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
 
@@ -117,9 +119,10 @@ static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t 
     p.counter_count = (int64_t)sk * p.cluster;
 }
 
-// Fill the shape-dependent fields for one kernel shape.
+// Fill the shape-dependent fields for one kernel shape.  `narrow_n` (path 3
+// only) is a C tile width of at most 64 columns, else 0 for 128.
 static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path,
-                       int32_t mma_n) {
+                       int32_t mma_n, int32_t narrow_n = 0) {
     p.path = path;
     p.mma_n = mma_n;
     p.cluster = (path == 4) ? 2 : 1;
@@ -132,7 +135,7 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
         p.tile_n = mma_n;
     } else {
         p.tile_m = mma_n;  // padded M
-        p.tile_n = 128;
+        p.tile_n = narrow_n > 0 ? narrow_n : 128;
     }
     p.tiles_m = (int32_t)((M + p.tile_m - 1) / p.tile_m);
     p.tiles_n = (int32_t)((N + p.tile_n - 1) / p.tile_n);
@@ -142,12 +145,23 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     // per CTA: B columns it loads (half of the tile for a pair)
     const int32_t b_cols = (path == 4) ? mma_n / 2 : mma_n;
     const int32_t b_bytes = b_cols * kBlockK * 2;
-    p.stage_bytes = kOperandABytes + b_bytes;
-    const int32_t stride = kOperandABytes + ((b_bytes + 1023) / 1024) * 1024;
-    int32_t stages = kStageBudget / stride;
+    // MMA A operand region per stage (a narrow swapped tile uses one chunk)
+    const bool narrow = (path == 3 && p.tile_n <= 64);
+    const int32_t a_region = narrow ? kOperandABytes / 2 : kOperandABytes;
+    // bytes the TMA copies of one stage deliver (boxes count in full)
+    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * kBlockK * 2 : kOperandABytes;
+    p.stage_bytes = a_box_bytes + b_bytes;
+    const int32_t stride = a_region + ((b_bytes + 1023) / 1024) * 1024;
+    const int32_t staging = (path == 3) ? 0 : kStagingBytes;
+    // a narrow tile's unused second chunk of the last stage reads up to
+    // 8 KiB past the ring: keep that much shared memory behind it
+    const int32_t tail_pad = narrow ? kOperandABytes / 2 : 0;
+    const int32_t budget = (path == 3) ? kSwapStageBudget - tail_pad
+                                       : kSmemLimit - kCtrlBytes - kAlignSlack - staging;
+    int32_t stages = budget / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     p.num_stages = stages;
-    p.smem_bytes = kCtrlBytes + kAlignSlack + stages * stride;
+    p.smem_bytes = kCtrlBytes + kAlignSlack + stages * stride + staging + tail_pad;
     int32_t cols = 2 * mma_n;
     int32_t alloc = 32;
     while (alloc < cols) alloc *= 2;
@@ -268,7 +282,25 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     if (want_swap) {
         // small M: C^T = B^T A^T, so N runs along the 128-wide MMA M side
         // and M (padded to 16) is the MMA N side.
-        take(3, (int32_t)((M + 15) / 16) * 16, num_sms);
+        const int32_t mpad = (int32_t)((M + 15) / 16) * 16;
+        // Narrow data-parallel tiles (8..64 columns, one TMA box per
+        // k-block) are only used when forced with "swapnW" (W = width):
+        // streaming B in strips narrower than 128 columns measured well
+        // below the bandwidth of 128-wide tiles split along K.
+        int32_t narrow = 0;
+        if (starts_with(f, "swapn"))
+            for (const char* d = f + 5; *d >= '0' && *d <= '9'; ++d) narrow = narrow * 10 + (*d - '0');
+        const bool use_narrow = narrow >= 8 && narrow <= 64 && narrow % 8 == 0;
+        if (use_narrow) {
+            gemm_relu_plan_t q;
+            memset(&q, 0, sizeof(q));
+            shape_plan(q, M, N, K, 3, mpad, narrow);
+            gemm_relu_plan_t r = q;
+            finish_split(r, q.num_tiles < num_sms ? q.num_tiles : num_sms, q.num_tiles, 0);
+            *plan = r;
+            return GEMM_OK;
+        }
+        take(3, mpad, num_sms);
     }
     if (want_pair) take(4, 256, pairs);
     if (want_t256) take(2, 256, num_sms);
