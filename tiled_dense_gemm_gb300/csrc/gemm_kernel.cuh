@@ -323,8 +323,7 @@ __device__ __forceinline__ void sink_direct_swap(__half* C, const float* v, int3
 template <int kMode>
 __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
     if constexpr (EpiTraits<kMode>::kChunk == 64) {
-        tmem_load_32cols(taddr, *reinterpret_cast<float(*)[32]>(v));
-        tmem_load_32cols(taddr + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+        tmem_load_64cols(taddr, *reinterpret_cast<float(*)[64]>(v));
     } else {
         tmem_load_16cols(taddr, *reinterpret_cast<float(*)[16]>(v));
     }

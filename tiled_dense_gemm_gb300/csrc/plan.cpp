@@ -19,39 +19,43 @@ constexpr int32_t kSwapStageBudget = 200 * 1024;
 constexpr int32_t kMaxStages = 16;
 constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
 
-// Cost model, in SM clock cycles.  Rough per-k-block costs of the three
-// kernel shapes; calibrated against measurements on GB300.
+// Cost model in microseconds, calibrated against GB300 measurements
+// (sm clock ~1.9-2.1 GHz): per-k-block mainloop time of each kernel shape,
+// the exposed part of a finished tile's store, and the split-K costs (fp32
+// partial write by a non-last CTA, and the last CTA's reduction per slot).
 struct Costs {
-    double kb;          // one k-block through the mainloop
-    double fill;        // CTA start: barrier init, TMEM alloc, pipeline fill
-    double tile_store;  // writing one finished fp16 tile
-    double partial;     // writing one fp32 partial tile
-    double reduce_per_slot;  // reading one partial during the fixup
+    double kb;               // one k-block through the mainloop
+    double fill;             // launch to first data: set-up and the first TMA round trip
+    double tile_store;       // storing one finished tile (TMEM -> C)
+    double partial;          // writing one fp32 partial tile
+    double reduce_per_slot;  // the last CTA's work per slot of a split tile
 };
 
 static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     Costs c;
-    const double tile_elems = 128.0 * mma_n;  // per CTA
-    if (path == 4) {
-        // a CTA pair: each CTA's tensor core does 128 x 256 x 64 per k-block
-        c.kb = 4.0 * 128.0 * 256.0 * 16.0 * 2.0 / 8192.0;
+    c.fill = 3.0;
+    if (path == 4) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
+        c.kb = 0.29;
+        c.tile_store = 2.5;
+        c.partial = 6.0;
+        c.reduce_per_slot = 4.0;
+    } else if (path == 2 && mma_n >= 256) {
+        c.kb = 0.37;
+        c.tile_store = 2.5;
+        c.partial = 6.0;
+        c.reduce_per_slot = 4.0;
     } else if (path == 2) {
-        // 4 MMAs of 128 x N x 16 per k-block; the tensor pipe does
-        // 8192 fp16 FLOP per SM per clock.  N = 128 is also bound by
-        // shared-memory bandwidth, hence the extra factor.
-        const double mma = 4.0 * 128.0 * mma_n * 16.0 * 2.0 / 8192.0;
-        c.kb = (mma_n >= 256) ? mma : mma * 1.2;
+        c.kb = 0.30;
+        c.tile_store = 1.3;
+        c.partial = 3.0;
+        c.reduce_per_slot = 2.0;
     } else {
-        // Swapped operands for small M: streaming B from HBM dominates.
-        // ~6.8 TB/s over 152 SMs at ~1.9 GHz is ~24 bytes per SM-clock.
-        const double mem = stage_bytes / 24.0;
-        const double mma = 4.0 * 128.0 * mma_n * 16.0 * 2.0 / 8192.0;
-        c.kb = mem > mma ? mem : mma;
+        // swapped operands, streaming B: ~0.4 us per 18 KiB stage per SM
+        c.kb = 0.40 * stage_bytes / 18432.0;
+        c.tile_store = 0.5;
+        c.partial = 1.0;
+        c.reduce_per_slot = 1.5;
     }
-    c.fill = 2500.0;
-    c.tile_store = tile_elems * 2.0 / 64.0;
-    c.partial = tile_elems * 4.0 / 64.0;
-    c.reduce_per_slot = tile_elems * 4.0 / 64.0;
     return c;
 }
 
@@ -170,7 +174,10 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
 
 // Choose the best split for the current shape over at most `workers`
 // persistent workers; returns its estimated cost.
-static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, int32_t force_splits) {
+static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, int32_t force_splits,
+                           bool operands_fit_l2) {
+    // a single tile row reads each B column block once whatever the order
+    operands_fit_l2 = operands_fit_l2 || p.tiles_m == 1;
     const Costs c = costs_for(p.path, p.mma_n, p.stage_bytes);
     const int32_t T = p.num_tiles;
     gemm_relu_plan_t best = p;
@@ -203,8 +210,11 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, i
         if (T >= workers) {
             const int32_t full = T / workers;
             if (T % workers != 0) consider(workers, (full - 1) * workers, T - (full - 1) * workers);
-        } else if (p.num_kb > 1) {
-            // fewer tiles than workers: split every tile along K over more workers
+        } else if (p.num_kb > 1 && operands_fit_l2) {
+            // fewer tiles than workers: split every tile along K over more
+            // workers.  Only when A and B stay in L2: the workers sharing a
+            // B column block then reach its rows at different times, and
+            // without L2 each would fetch it from DRAM again.
             for (int32_t g = T + 1; g <= workers; ++g) consider(g, 0, T);
         }
     }
@@ -253,7 +263,11 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         }
     int32_t pairs = (max_pairs > 0 && max_pairs < num_sms / 2) ? max_pairs : num_sms / 2;
 
-    bool want_swap = M <= 128, want_t256 = M > 128, want_t128 = M > 128, want_pair = M > 128 && pairs > 0;
+    // A + B small enough to stay resident in the 126 MiB L2 next to C
+    const bool operands_fit_l2 = 2.0 * ((double)M * K + (double)K * N) <= 48.0 * 1024 * 1024;
+    // small M: the swapped-operand kernel (MMA N = padded M) for M <= 32;
+    // above that the 128 x 128 tiled kernel measured faster
+    bool want_swap = M <= 32, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
     if (starts_with(f, "swap") && M <= 128) {
         want_t256 = want_t128 = want_pair = false;
         want_swap = true;
@@ -273,7 +287,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         gemm_relu_plan_t q;
         memset(&q, 0, sizeof(q));
         shape_plan(q, M, N, K, path, mma_n);
-        const double cost = choose_split(q, workers, dp_only, force_splits);
+        const double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2);
         if (best_cost < 0.0 || cost < best_cost) {
             best_cost = cost;
             *plan = q;
@@ -298,6 +312,22 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
             gemm_relu_plan_t r = q;
             finish_split(r, q.num_tiles < num_sms ? q.num_tiles : num_sms, q.num_tiles, 0);
             *plan = r;
+            return GEMM_OK;
+        }
+        // Streaming B: cut each 128-column tile into S equal K ranges with
+        // S = SMs / tiles (tile-fastest item order, so CTAs running together
+        // sweep whole rows of B), when that keeps >= 3/4 of the SMs busy;
+        // otherwise let the cost model pick data-parallel or stream-K.
+        gemm_relu_plan_t q;
+        memset(&q, 0, sizeof(q));
+        shape_plan(q, M, N, K, 3, mpad);
+        // (S <= 4: the last CTA of a tile reads the other S - 1 partials)
+        const int32_t sp = q.num_tiles > 0 ? num_sms / q.num_tiles : 0;
+        if (force_splits <= 1 && !dp_only && !starts_with(f, "swap") && sp >= 2 && sp <= 4 &&
+            sp <= q.num_kb && 4 * q.num_tiles * sp >= 3 * num_sms) {
+            finish_split(q, q.num_tiles * sp, 0, q.num_tiles, sp);
+            q.grid = q.num_tiles * sp;
+            *plan = q;
             return GEMM_OK;
         }
         take(3, mpad, num_sms);
