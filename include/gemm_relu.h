@@ -171,8 +171,11 @@ typedef struct {
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
  * "tiled256", "tiled128", "swap" (M <= 128 only), "swapnW" (M <= 128,
  * data-parallel tiles W = 8..64 columns wide) or "pair", optionally
- * followed by ":dp" to forbid splitting tiles along K, or by ":sN" to cut
- * every tile into N equal K ranges (the split schedule).
+ * followed by ":dp" to forbid splitting tiles along K, by ":sN" to cut
+ * every tile into N equal K ranges (the split schedule), or by ":c2" to
+ * split every tile's K range between the two CTAs of a cluster, which
+ * combine their halves through distributed shared memory ("pair" has no
+ * ":c2": its cluster already holds one 256-row tile).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);

@@ -33,13 +33,17 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["path"] == 2
     else:
         assert d["path"] in (2, 4)
+    csk = d["path"] in (2, 3) and d["cluster"] > 1  # cluster split-K
+    if csk:
+        assert d["cluster"] == 2 and d["dp_tiles"] == d["num_tiles"] == d["grid"]
+        assert d["sk_tiles"] == 0 and d["workspace_bytes"] == 0
     if d["path"] == 3:
         assert d["mma_n"] == ((M + 15) // 16) * 16
         assert d["tile_n"] == 128 or (8 <= d["tile_n"] <= 64 and d["tile_n"] % 8 == 0 and d["sk_tiles"] == 0)
-        assert d["mma_m"] == 128 and d["cluster"] == 1
+        assert d["mma_m"] == 128 and (d["cluster"] == 1 or csk)
     elif d["path"] == 2:
         assert d["mma_n"] in (128, 256) and d["tile_m"] == 128
-        assert d["mma_m"] == 128 and d["cluster"] == 1
+        assert d["mma_m"] == 128 and (d["cluster"] == 1 or csk)
     else:
         assert (d["mma_m"], d["mma_n"], d["tile_m"], d["tile_n"], d["cluster"]) == (256, 256, 256, 256, 2)
         assert d["stage_bytes"] == 32768
@@ -58,7 +62,8 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     slots = defaultdict(dict)
     coords = {}
     sk_units = []
-    for cta in range(d["grid"]):
+    n_cta = d["grid"] * d["cluster"] if csk else d["grid"]
+    for cta in range(n_cta):
         items = gemm_lib.plan_work_items(p, cta)
         units = 0
         for it in items:
@@ -69,7 +74,12 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
             coords[it["tile"]] = (it["tm"], it["tn"])
             for kb in range(it["kb0"], it["kb1"]):
                 cover[(it["tile"], kb)] += 1
-            if it["tile"] < d["dp_tiles"]:
+            if csk:
+                r = cta % d["cluster"]
+                assert it["slot"] == r and it["nslots"] == d["cluster"]
+                assert it["kb0"] == r * d["num_kb"] // d["cluster"]
+                assert it["kb1"] == (r + 1) * d["num_kb"] // d["cluster"]
+            elif it["tile"] < d["dp_tiles"]:
                 assert (it["kb0"], it["kb1"], it["nslots"]) == (0, d["num_kb"], 1)
             else:
                 units += it["kb1"] - it["kb0"]
@@ -108,7 +118,7 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
                                    "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3", "swapn56",
-                                   "swapn8"])
+                                   "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256)}
@@ -120,6 +130,8 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert (d["path"], d["mma_n"]) == want[force.split(":")[0]]
         if force.endswith(":dp"):
             assert d["sk_tiles"] == 0
+        if ":c2" in force and d["num_tiles"] <= 76 and d["num_kb"] >= 2:
+            assert d["cluster"] == 2 and d["grid"] == d["num_tiles"]
         if ":s" in force:
             want_s = min(int(force.split(":s")[1]), d["num_kb"])
             assert d["dp_tiles"] == 0 and d["max_slots"] == want_s
@@ -149,6 +161,6 @@ def test_headline_shapes_use_the_intended_kernels(gemm_lib):
     sq = gemm_lib.plan(4096, 4096, 4096, 152)
     assert sq.path == 4 and sq.grid == 76 and sq.cluster == 2
     sk = gemm_lib.plan(16, 8192, 8192, 152)
-    # 64 tiles of 128 columns, each cut into 2 K ranges: 128 CTAs
+    # 64 tiles of 128 columns, each by a 2-CTA cluster (one K half each)
     assert sk.path == 3 and sk.mma_n == 16 and sk.tile_n == 128
-    assert sk.splits == 2 and sk.grid == 128 and sk.dp_tiles == 0
+    assert sk.cluster == 2 and sk.grid == 64 and sk.dp_tiles == 64

@@ -57,6 +57,7 @@ struct __align__(8) Ctrl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t final_bar;
+    uint64_t exch_bar;  // cluster split-K: the peers' partials are ready (rank 0)
     uint32_t tmem_addr;
     int32_t abort_flag;
     int32_t last_flag;
@@ -137,40 +138,59 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 // adding to their start-address field (a 14-bit field of 16-byte units that
 // cannot carry: shared addresses stay below 256 KiB).
 
+// The TMA producer: one thread walks the work items and k-blocks, waits for
+// a free ring stage, and issues the stage's copies.  issue() keeps its
+// position between calls.
 template <int kMode>
-__device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
-                                              uint32_t stride, uint32_t a_bytes, const CUtensorMap* tmA,
-                                              const CUtensorMap* tmB, int32_t worker) {
+struct Producer {
     using T = ModeTraits<kMode>;
-    const gemm_relu_plan_t pl = p.plan;
-    const uint32_t S = (uint32_t)pl.num_stages;
-    const uint32_t full0 = smem_u32(&ctrl->full[0]);
-    const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
-    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
-    // a pair's copies all complete on the leader's barrier, which expects
-    // the bytes of both CTAs
-    const uint32_t tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
-    const int32_t tile_m = pl.tile_m;
-    const int32_t tile_n = pl.tile_n;
+    const KParams& p;
+    Ctrl* ctrl;
+    const CUtensorMap* tmA;
+    const CUtensorMap* tmB;
+    gemm_relu_plan_t pl;
+    uint32_t stages, stride, a_bytes, rank, S, full0, empty0, tx_bytes;
     WorkIter wi;
-    wi.init(pl, worker);
     WorkItem w;
-    uint32_t s = 0, ph = 0;
-    while (wi.next(pl, w)) {
-        // first row of A and first column of B this CTA loads for the tile
-        int32_t a_row, b_col;
-        if constexpr (T::kPair) {
-            a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
-            b_col = w.tn * (int32_t)T::kBN + 128 * (int32_t)rank;
-        } else if constexpr (!T::kSwap) {
-            a_row = w.tm * 128;
-            b_col = w.tn * (int32_t)T::kBN;
-        } else {
-            a_row = w.tm * tile_m;
-            b_col = w.tn * tile_n;
-        }
-        for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-            if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return;
+    bool have_item;
+    int32_t kb, a_row, b_col;
+    uint32_t s, ph;
+
+    __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
+                                        uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
+                                        int32_t worker, uint32_t rank_)
+        : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), pl(p_.plan), stages(stages_), stride(stride_),
+          a_bytes(a_bytes_), rank(rank_), have_item(false), kb(0), a_row(0), b_col(0), s(0), ph(0) {
+        S = (uint32_t)pl.num_stages;
+        full0 = smem_u32(&ctrl->full[0]);
+        empty0 = smem_u32(&ctrl->empty[0]);
+        // a pair's copies all complete on the leader's barrier, which
+        // expects the bytes of both CTAs
+        tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
+        wi.init(pl, worker, (int32_t)rank);
+    }
+
+    // Issue up to `budget` k-blocks of copies (all remaining if < 0).
+    // Returns false if the CTA is aborting.
+    __device__ __forceinline__ bool issue(int32_t budget) {
+        while (budget != 0) {
+            if (!have_item || kb == w.kb1) {
+                if (!wi.next(pl, w)) return true;
+                have_item = true;
+                kb = w.kb0;
+                // first row of A and first column of B this CTA loads
+                if constexpr (T::kPair) {
+                    a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
+                    b_col = w.tn * (int32_t)T::kBN + 128 * (int32_t)rank;
+                } else if constexpr (!T::kSwap) {
+                    a_row = w.tm * 128;
+                    b_col = w.tn * (int32_t)T::kBN;
+                } else {
+                    a_row = w.tm * pl.tile_m;
+                    b_col = w.tn * pl.tile_n;
+                }
+            }
+            if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return false;
             const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
@@ -194,7 +214,7 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
                     // per TMA box (a narrow tile fills part of one chunk; the
                     // accumulator lanes past tile_n are never stored)
                     tma_load_2d(a_dst, tmB, full, b_col, k0);
-                    if (tile_n > 64) tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
+                    if (pl.tile_n > 64) tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
                     // MMA B operand: the (padded) rows of A
                     tma_load_2d(b_dst, tmA, full, k0, a_row);
                 }
@@ -203,14 +223,17 @@ __device__ __forceinline__ void producer_role(const KParams& p, Ctrl* ctrl, uint
                 s = 0;
                 ph ^= 1u;
             }
+            ++kb;
+            if (budget > 0) --budget;
         }
+        return true;
     }
-}
+};
 
 template <int kMode>
 __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t stages,
                                          uint32_t stride, uint32_t a_bytes, uint32_t tmem_base,
-                                         int32_t worker) {
+                                         int32_t worker, uint32_t rank) {
     using T = ModeTraits<kMode>;
     const gemm_relu_plan_t pl = p.plan;
     const uint32_t S = (uint32_t)pl.num_stages;
@@ -231,7 +254,7 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     constexpr uint32_t kBStep = (T::kSwap ? 32u : 2 * kAtomBytes) >> 4;
     const uint32_t stride16 = stride >> 4;
     WorkIter wi;
-    wi.init(pl, worker);
+    wi.init(pl, worker, (int32_t)rank);
     WorkItem w;
     uint32_t s = 0, ph = 0, local = 0;
     while (wi.next(pl, w)) {
@@ -331,8 +354,8 @@ __device__ __forceinline__ void tmem_load_chunk(uint32_t taddr, float* v) {
 
 template <int kMode>
 __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint32_t tmem_base,
-                                              int32_t worker, const CUtensorMap* tmC,
-                                              uint32_t staging) {
+                                              int32_t worker, uint32_t rank, const CUtensorMap* tmC,
+                                              uint32_t stages, uint32_t staging) {
     using T = ModeTraits<kMode>;
     constexpr int kChunk = EpiTraits<kMode>::kChunk;
     constexpr int kQ = kChunk / 4;  // float4 groups per chunk
@@ -343,8 +366,8 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     float* const ws = p.ws;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
-    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
     const uint32_t lane_row = quarter * 32 + lane;  // TMEM lane = accumulator row
+    const uint32_t half = T::kPair ? rank : 0u;      // which 128 rows of a pair tile
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
     const int64_t tile_elems = (int64_t)128 * ncols;
@@ -352,7 +375,7 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     uint32_t sbuf = 0;
     volatile int32_t* last_flag = &ctrl->last_flag;
     WorkIter wi;
-    wi.init(pl, worker);
+    wi.init(pl, worker, (int32_t)rank);
     WorkItem w;
     uint32_t local = 0;
     float v[kChunk];
@@ -364,7 +387,7 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
                 sink_direct_swap(C, v, apply_relu, (int64_t)it.tn * pl.tile_n + lane_row,
                                  (int64_t)it.tm * pl.tile_m + c, M, N);
         } else {
-            const int64_t row0 = (int64_t)it.tm * T::kTileM + 128 * rank + 32 * quarter;
+            const int64_t row0 = (int64_t)it.tm * T::kTileM + 128 * half + 32 * quarter;
             const int64_t col = (int64_t)it.tn * T::kBN + c;
             sink_tma(tmC, my_staging + sbuf * 4096u, lane, v, apply_relu, col, row0, M, N);
             sbuf ^= 1u;
@@ -409,6 +432,71 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
         // columns interleaved by lane:
         //   element (col, lane) at ((col / 4) * 128 + lane) * 4 + col % 4
         // so a warp writes / reads 512 contiguous bytes per instruction.
+        if (cluster_split(pl)) {
+            // Cluster split-K.  Each CTA holds one K range of this tile (its
+            // only item, so its ring is idle).  Ranks > 0 leave their fp32
+            // accumulator in their own ring, lane-interleaved float4 groups
+            // as for global partials, and signal rank 0; rank 0 adds them
+            // to its own in rank order, reading them over DSMEM.  The
+            // cluster barrier at teardown keeps the ranks alive until then.
+            const uint32_t exch = smem_u32(&ctrl->exch_bar);
+            if (rank != 0) {
+                for (uint32_t c = 0; c < ncols; c += kChunk) {
+                    __syncwarp();
+                    tmem_load_chunk<kMode>(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j)
+                        st_shared_v4(stages + (((c / 4 + j) * 128u + lane_row) << 4),
+                                     make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                                __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])));
+                }
+                release_tmem();
+                fence_acq_rel_cluster();
+                named_bar_sync(kEpiBarrier, kEpiThreads);
+                if (threadIdx.x == 64) mbar_arrive_cluster(mapa_shared(exch, 0));
+                ++local;
+                continue;
+            }
+            bool ready = true;
+            {
+                const uint64_t t0 = globaltimer_ns();
+                volatile int32_t* abort_flag = &ctrl->abort_flag;
+                while (!mbar_try_wait_acq_cluster(exch, 0)) {
+                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                        *abort_flag = 1;
+                        atomicCAS(p.err, 0, kErrEpilogue);
+                        ready = false;
+                        break;
+                    }
+                }
+            }
+            ready = named_bar_and(kEpiBarrier, kEpiThreads, ready);
+            if (!ready) {
+                release_tmem();
+                break;
+            }
+            for (uint32_t c = 0; c < ncols; c += kChunk) {
+                __syncwarp();
+                tmem_load_chunk<kMode>(taddr + c, v);  // rank 0's share
+                for (uint32_t r = 1; r < (uint32_t)pl.cluster; ++r) {
+                    float4 x[kQ];
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j)
+                        x[j] = ld_shared_cluster_f4(mapa_shared(stages + (((c / 4 + j) * 128u + lane_row) << 4), r));
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) {
+                        v[4 * j] += x[j].x;
+                        v[4 * j + 1] += x[j].y;
+                        v[4 * j + 2] += x[j].z;
+                        v[4 * j + 3] += x[j].w;
+                    }
+                }
+                sink(w, c);
+            }
+            release_tmem();
+            ++local;
+            continue;
+        }
         const int64_t split_id = T::kPair ? (int64_t)w.sk_index * 2 + rank : (int64_t)w.sk_index;
         uint32_t* const counter = p.counters + split_id;
         uint32_t* const flags = p.counters + pl.counter_count + split_id * pl.max_slots;
@@ -531,8 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t rank = T::kPair ? cluster_ctarank() : 0u;
-    const int32_t worker = T::kPair ? (int32_t)(blockIdx.x / 2) : (int32_t)blockIdx.x;
+    // CTA pairs (one MMA for two CTAs) and cluster split-K run in clusters
+    const bool clustered = T::kPair || cluster_split(pl);
+    const uint32_t rank = clustered ? cluster_ctarank() : 0u;
+    const int32_t worker = clustered ? (int32_t)(blockIdx.x / (uint32_t)pl.cluster) : (int32_t)blockIdx.x;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -548,6 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctrl->tmem_empty[b]), (T::kPair ? 2u : 1u) * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctrl->final_bar), 1);
+        mbar_init(smem_u32(&ctrl->exch_bar), pl.cluster > 1 ? (uint32_t)pl.cluster - 1u : 1u);
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
         fence_mbar_init();
@@ -557,19 +648,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish<T::kCG>();
     }
     tc_fence_before();
-    if constexpr (T::kPair)
-        cluster_sync();  // the peer's barriers are initialised before any remote arrive
+    if (clustered)
+        cluster_sync();  // the peers' barriers are initialised before any remote arrive
     else
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_addr;
 
     if (warp == 0) {
-        if (lane == 0) producer_role<kMode>(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, worker);
+        if (lane == 0) {
+            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, worker, rank);
+            prod.issue(-1);
+        }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {  // one thread of the (leader) CTA issues every MMA
-            mma_role<kMode>(p, ctrl, stages, stride, a_bytes, tmem_base, worker);
+        if (lane == 0 && (!T::kPair || rank == 0)) {  // one thread (of a pair's leader) issues the MMAs
+            mma_role<kMode>(p, ctrl, stages, stride, a_bytes, tmem_base, worker, rank);
             // no MMA may still be running when tensor memory is released
             mma_commit<T::kCG>(smem_u32(&ctrl->final_bar), 0x1);
             if (!wait_phase_for(smem_u32(&ctrl->final_bar), 0, p.timeout_ns)) atomicCAS(p.err, 0, kErrFinal);
@@ -578,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // C staging for the TMA stores sits after the ring (tiled paths)
         const uint32_t staging = stages + (uint32_t)pl.num_stages * stride;
-        epilogue_role<kMode>(p, ctrl, tmem_base, worker, &tmC, staging);
+        epilogue_role<kMode>(p, ctrl, tmem_base, worker, rank, &tmC, stages, staging);
     }
 
     if (warp == 0 && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
@@ -589,8 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     tc_fence_before();
-    if constexpr (T::kPair)
-        cluster_sync();  // the peer's shared memory is read by the pair's MMAs until here
+    if (clustered)
+        cluster_sync();  // a peer's shared memory may be read (MMA, DSMEM) until here
     else
         __syncthreads();
     if (warp == 1) {

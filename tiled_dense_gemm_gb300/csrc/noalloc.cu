@@ -137,7 +137,7 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     NoAllocState& s = g_na[dev];
 
     gemm_relu_plan_t pl;
-    rc = plan_problem(M, N, K, s.sm_count, 0, "swap", &pl);
+    rc = plan_problem(M, N, K, s.sm_count, -1, "swap", &pl);  // no clusters: plain launch
     if (rc != GEMM_OK) return rc;
     if (pl.path != 3) return GEMM_ERR_TOO_LARGE;
     const size_t partial_bytes = (size_t)pl.workspace_bytes;

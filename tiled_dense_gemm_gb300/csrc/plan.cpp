@@ -15,7 +15,7 @@ constexpr int32_t kCtrlBytes = 1024;        // barriers + flags
 constexpr int32_t kAlignSlack = 1024;       // dynamic smem rounded up to 1 KiB
 constexpr int32_t kSmemLimit = 227 * 1024;  // opt-in shared memory per CTA
 constexpr int32_t kStagingBytes = 32 * 1024;  // C staging for TMA stores (tiled paths)
-constexpr int32_t kSwapStageBudget = 200 * 1024;
+constexpr int32_t kSwapStageBudget = kSmemLimit - kCtrlBytes - kAlignSlack;  // no C staging
 constexpr int32_t kMaxStages = 16;
 constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
 
@@ -29,11 +29,15 @@ struct Costs {
     double tile_store;       // storing one finished tile (TMEM -> C)
     double partial;          // writing one fp32 partial tile
     double reduce_per_slot;  // the last CTA's work per slot of a split tile
+    double exchange;         // cluster split-K: reading the peer's fp32 tile over DSMEM
 };
 
 static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     Costs c;
     c.fill = 3.0;
+    // measured: ~1 us of handshake + the peer's 128 x mma_n fp32 tile at
+    // ~32 B/clk over DSMEM, plus the cluster teardown
+    c.exchange = 1.0 + 128.0 * mma_n * 4.0 / 32000.0;
     if (path == 4) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
         c.kb = 0.29;
         c.tile_store = 2.5;
@@ -175,7 +179,7 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
 // Choose the best split for the current shape over at most `workers`
 // persistent workers; returns its estimated cost.
 static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, int32_t force_splits,
-                           bool operands_fit_l2) {
+                           bool operands_fit_l2, int32_t pairs = 0) {
     // a single tile row reads each B column block once whatever the order
     operands_fit_l2 = operands_fit_l2 || p.tiles_m == 1;
     const Costs c = costs_for(p.path, p.mma_n, p.stage_bytes);
@@ -206,6 +210,19 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, i
     }
     // plain data-parallel
     consider(T < workers ? T : workers, T, 0);
+    // cluster split-K: each tile by a cluster of 2 CTAs, one K half each,
+    // combined through distributed shared memory; one wave of clusters
+    if (!dp_only && pairs > 0 && p.path != 4 && T <= pairs && p.num_kb >= 8) {
+        gemm_relu_plan_t q = p;
+        finish_split(q, T, T, 0);
+        q.cluster = 2;
+        q.max_slots = 2;
+        double cost = c.fill + (double)((p.num_kb + 1) / 2) * c.kb + c.tile_store + c.exchange;
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
+            best = q;
+        }
+    }
     if (!dp_only) {
         if (T >= workers) {
             const int32_t full = T / workers;
@@ -255,13 +272,16 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
 
     const char* f = force ? force : "";
     const bool dp_only = contains(f, ":dp");
+    const bool force_csk = contains(f, ":c2");
     int32_t force_splits = 0;
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 's' && q[2] >= '0' && q[2] <= '9') {
             force_splits = 0;
             for (const char* d = q + 2; *d >= '0' && *d <= '9'; ++d) force_splits = force_splits * 10 + (*d - '0');
         }
+    // co-resident 2-CTA clusters (CTA pairs, cluster split-K); < 0: none
     int32_t pairs = (max_pairs > 0 && max_pairs < num_sms / 2) ? max_pairs : num_sms / 2;
+    if (max_pairs < 0) pairs = 0;
 
     // A + B small enough to stay resident in the 126 MiB L2 next to C
     const bool operands_fit_l2 = 2.0 * ((double)M * K + (double)K * N) <= 48.0 * 1024 * 1024;
@@ -287,7 +307,13 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         gemm_relu_plan_t q;
         memset(&q, 0, sizeof(q));
         shape_plan(q, M, N, K, path, mma_n);
-        const double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2);
+        double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2, pairs);
+        if (force_csk && pairs > 0 && path != 4 && q.num_tiles <= pairs && q.num_kb >= 2) {
+            finish_split(q, q.num_tiles, q.num_tiles, 0);
+            q.cluster = 2;
+            q.max_slots = 2;
+            cost = 0.0;
+        }
         if (best_cost < 0.0 || cost < best_cost) {
             best_cost = cost;
             *plan = q;
@@ -323,6 +349,15 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         shape_plan(q, M, N, K, 3, mpad);
         // (S <= 4: the last CTA of a tile reads the other S - 1 partials)
         const int32_t sp = q.num_tiles > 0 ? num_sms / q.num_tiles : 0;
+        if (force_splits <= 1 && !dp_only && !starts_with(f, "swap") && sp >= 2 && pairs > 0 &&
+            q.num_tiles <= pairs && q.num_kb >= 8 && 4 * q.num_tiles * 2 >= 3 * num_sms) {
+            // two K halves per tile in one 2-CTA cluster: no global partials
+            finish_split(q, q.num_tiles, q.num_tiles, 0);
+            q.cluster = 2;
+            q.max_slots = 2;
+            *plan = q;
+            return GEMM_OK;
+        }
         if (force_splits <= 1 && !dp_only && !starts_with(f, "swap") && sp >= 2 && sp <= 4 &&
             sp <= q.num_kb && 4 * q.num_tiles * sp >= 3 * num_sms) {
             finish_split(q, q.num_tiles * sp, 0, q.num_tiles, sp);
@@ -350,9 +385,17 @@ extern "C" int gemm_relu_plan_work_item(const gemm_relu_plan_t* plan, int cta, i
                                         int32_t* kb_begin, int32_t* kb_end, int32_t* slot,
                                         int32_t* nslots) {
     using namespace gr;
-    if (!plan || cta < 0 || idx < 0 || plan->path < 2 || cta >= plan->grid) return -1;
+    // `cta` is the worker index, except for cluster split-K plans, where it
+    // is the CTA index (worker * cluster + rank)
+    if (!plan) return -1;
+    const bool csk = cluster_split(*plan);
+    const int32_t ctas = csk ? plan->grid * plan->cluster : plan->grid;
+    if (cta < 0 || idx < 0 || plan->path < 2 || cta >= ctas) return -1;
     WorkIter wi;
-    wi.init(*plan, cta);
+    if (csk)
+        wi.init(*plan, cta / plan->cluster, cta % plan->cluster);
+    else
+        wi.init(*plan, cta);
     WorkItem w;
     for (int i = 0; i <= idx; ++i)
         if (!wi.next(*plan, w)) return 0;

@@ -65,13 +65,23 @@ struct WorkItem {
     int32_t sk_index;  // stream-K tile index (tile - dp_tiles), -1 when data-parallel
 };
 
+// Cluster split-K: a one-CTA kernel shape (path 2 or 3) launched in
+// clusters of `cluster` CTAs, each cluster one worker; CTA rank r of the
+// cluster computes K range r of every tile of the worker, and the CTAs
+// combine their accumulators through distributed shared memory.
+GR_HD bool cluster_split(const gemm_relu_plan_t& p) {
+    return (p.path == 2 || p.path == 3) && p.cluster > 1;
+}
+
 struct WorkIter {
     int32_t cta;
+    int32_t rank;  // CTA rank in the cluster (cluster split-K); 0 otherwise
     int32_t dp_i, dp_n;
     int64_t u, u1;  // stream-K units, or split items when p.splits > 1
 
-    GR_HD void init(const gemm_relu_plan_t& p, int32_t c) {
+    GR_HD void init(const gemm_relu_plan_t& p, int32_t c, int32_t r = 0) {
         cta = c;
+        rank = cluster_split(p) ? r : 0;
         dp_i = 0;
         dp_n = (c < p.dp_tiles) ? (p.dp_tiles - 1 - c) / p.grid + 1 : 0;
         if (p.sk_tiles > 0 && p.splits > 1) {
@@ -88,11 +98,18 @@ struct WorkIter {
     GR_HD bool next(const gemm_relu_plan_t& p, WorkItem& w) {
         if (dp_i < dp_n) {
             w.tile = cta + dp_i * p.grid;
-            w.kb0 = 0;
-            w.kb1 = p.num_kb;
-            w.slot = 0;
-            w.nslots = 1;
             w.sk_index = -1;
+            if (cluster_split(p)) {
+                w.kb0 = (int32_t)((int64_t)rank * p.num_kb / p.cluster);
+                w.kb1 = (int32_t)((int64_t)(rank + 1) * p.num_kb / p.cluster);
+                w.slot = rank;
+                w.nslots = p.cluster;
+            } else {
+                w.kb0 = 0;
+                w.kb1 = p.num_kb;
+                w.slot = 0;
+                w.nslots = 1;
+            }
             ++dp_i;
             tile_coords(p, w.tile, w.tm, w.tn);
             return true;
