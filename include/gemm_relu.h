@@ -143,7 +143,8 @@ typedef struct {
     int32_t tile_m;      /* C tile rows */
     int32_t tile_n;      /* C tile columns */
     int32_t tiles_m, tiles_n, num_tiles;
-    int32_t num_kb;      /* ceil(K / 64) */
+    int32_t num_kb;      /* ceil(K / block_k) */
+    int32_t block_k;     /* k-rows per shared-memory ring stage: 64, or 128 for path 3 */
     int32_t group_m;     /* tile rasterisation: tiles_m are walked in groups of group_m */
     int32_t grid;        /* persistent workers (a worker is `cluster` CTAs) */
     int32_t cluster;     /* CTAs per worker: 1, or 2 for path 4 */
@@ -175,7 +176,8 @@ typedef struct {
  * every tile into N equal K ranges (the split schedule), or by ":c2" to
  * split every tile's K range between the two CTAs of a cluster, which
  * combine their halves through distributed shared memory ("pair" has no
- * ":c2": its cluster already holds one 256-row tile).
+ * ":c2": its cluster already holds one 256-row tile), or by ":sk" to run
+ * every tile stream-K over all workers.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);

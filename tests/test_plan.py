@@ -29,6 +29,9 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["path"] in (2, 3, 4)
     elif M <= 32:
         assert d["path"] == 3  # swapped operands for very small M
+    elif M <= 64:
+        # swapped operands only with a cluster or plain split of K
+        assert d["path"] == 2 or (d["path"] == 3 and (d["cluster"] == 2 or d["splits"] > 1))
     elif M <= 128:
         assert d["path"] == 2
     else:
@@ -49,7 +52,8 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["stage_bytes"] == 32768
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
     assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
-    assert d["num_kb"] == (K + 63) // 64
+    assert d["block_k"] == (128 if d["path"] == 3 else 64)
+    assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
     assert d["smem_bytes"] <= SMEM_LIMIT
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
@@ -118,7 +122,8 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
                                    "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3", "swapn56",
-                                   "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2"])
+                                   "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk",
+                                   "tiled128:sk"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256)}
@@ -132,7 +137,11 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert d["sk_tiles"] == 0
         if ":c2" in force and d["num_tiles"] <= 76 and d["num_kb"] >= 2:
             assert d["cluster"] == 2 and d["grid"] == d["num_tiles"]
-        if ":s" in force:
+        if force.endswith(":sk"):
+            assert d["dp_tiles"] == 0 and d["sk_tiles"] == d["num_tiles"] and d["splits"] == 1
+            workers = 76 if d["path"] == 4 else 152  # CTA pairs on 152 SMs
+            assert d["grid"] == min(workers, d["num_tiles"] * d["num_kb"])
+        elif ":s" in force:
             want_s = min(int(force.split(":s")[1]), d["num_kb"])
             assert d["dp_tiles"] == 0 and d["max_slots"] == want_s
             assert d["splits"] == (want_s if want_s > 1 else 1)

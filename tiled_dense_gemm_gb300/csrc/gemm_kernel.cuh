@@ -88,6 +88,9 @@ struct ModeTraits {
     static constexpr uint32_t kBN = (kMode == 1) ? 128 : 256;  // C columns per tile (normal)
     static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
     static constexpr uint32_t kBCols = kPair ? 128 : kBN;      // B columns loaded per CTA
+    // k-rows per ring stage (the plan's block_k): the swapped kernel's
+    // small MMAs take 128 per stage, the others 64
+    static constexpr uint32_t kBK = kSwap ? 2 * kBlockK : kBlockK;
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
@@ -155,6 +158,11 @@ struct Producer {
     bool have_item;
     int32_t kb, a_row, b_col;
     uint32_t s, ph;
+    // an operand that only one row (column) of tiles reads is streamed
+    // through L2 exactly once: its lines go first
+    bool once_a, once_b;
+    uint64_t pol_first;
+    uint32_t a_sub_bytes;  // swapped: bytes of one 64-k box of A's padded rows
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
@@ -167,6 +175,10 @@ struct Producer {
         // a pair's copies all complete on the leader's barrier, which
         // expects the bytes of both CTAs
         tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
+        a_sub_bytes = (uint32_t)pl.tile_m * kSwizzleRow;
+        once_a = pl.tiles_n == 1;
+        once_b = pl.tiles_m == 1;
+        pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
     }
 
@@ -194,7 +206,7 @@ struct Producer {
             const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
-            const int32_t k0 = kb * kBlockK;
+            const int32_t k0 = kb * (int32_t)T::kBK;
             if constexpr (T::kPair) {
                 const uint32_t full_leader = mapa_shared(full, 0);
                 if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
@@ -205,18 +217,24 @@ struct Producer {
             } else {
                 mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
-                    tma_load_2d(a_dst, tmA, full, k0, a_row);
+                    tma_load_2d_maybe_hint(a_dst, tmA, full, k0, a_row, once_a, pol_first);
 #pragma unroll
                     for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                        tma_load_2d(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0);
+                        tma_load_2d_maybe_hint(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0,
+                                               once_b, pol_first);
                 } else {
                     // MMA A operand: the tile's columns of B, one 64-wide chunk
-                    // per TMA box (a narrow tile fills part of one chunk; the
-                    // accumulator lanes past tile_n are never stored)
-                    tma_load_2d(a_dst, tmB, full, b_col, k0);
-                    if (pl.tile_n > 64) tma_load_2d(a_dst + kChunkBytes, tmB, full, b_col + 64, k0);
-                    // MMA B operand: the (padded) rows of A
-                    tma_load_2d(b_dst, tmA, full, k0, a_row);
+                    // of kBK k-rows per TMA box (a narrow tile fills part of
+                    // one chunk)
+                    constexpr uint32_t kSwapChunk = T::kBK * kSwizzleRow;
+                    tma_load_2d_maybe_hint(a_dst, tmB, full, b_col, k0, once_b, pol_first);
+                    if (pl.tile_n > 64)
+                        tma_load_2d_maybe_hint(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b, pol_first);
+                    // MMA B operand: the (padded) rows of A, one box per 64 k
+#pragma unroll
+                    for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
+                        tma_load_2d_maybe_hint(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                               once_a, pol_first);
                 }
             }
             if (++s == S) {
@@ -246,12 +264,15 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     // Descriptors of stage 0 and per-16-k advances, in 16-byte units.
     // K-major operand (A; A^T when swapped): +32 bytes inside the swizzled
     // row.  MN-major operand (B; B^T when swapped): +16 k-rows = 2 atoms.
-    const uint64_t a_desc0 = T::kSwap ? make_sw128_desc(stages, kChunkBytes, kAtomBytes)
+    // Swapped: the B^T chunks are kBK k-rows long; A^T is one 64-k box of
+    // the padded rows per 64 k, so its k16 step also hops boxes.
+    const uint64_t a_desc0 = T::kSwap ? make_sw128_desc(stages, T::kBK * kSwizzleRow, kAtomBytes)
                                       : make_sw128_desc(stages, 16, kAtomBytes);
     const uint64_t b_desc0 = T::kSwap ? make_sw128_desc(stages + a_bytes, 16, kAtomBytes)
                                       : make_sw128_desc(stages + a_bytes, kChunkBytes, kAtomBytes);
     constexpr uint32_t kAStep = (T::kSwap ? 2 * kAtomBytes : 32u) >> 4;
     constexpr uint32_t kBStep = (T::kSwap ? 32u : 2 * kAtomBytes) >> 4;
+    const uint32_t b_box16 = ((uint32_t)pl.tile_m * kSwizzleRow) >> 4;  // swapped: one 64-k box of A
     const uint32_t stride16 = stride >> 4;
     WorkIter wi;
     wi.init(pl, worker, (int32_t)rank);
@@ -270,9 +291,11 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
             const uint64_t b_desc = b_desc0 + (uint64_t)(s * stride16);
             const uint32_t acc = (kb > w.kb0) ? 1u : 0u;
 #pragma unroll
-            for (uint32_t k = 0; k < kBlockK / 16; ++k)
-                mma_f16_ss<T::kCG>(d_tmem, a_desc + k * kAStep, b_desc + k * kBStep, idesc,
-                                   k > 0 ? 1u : acc);
+            for (uint32_t k = 0; k < T::kBK / 16; ++k) {
+                const uint64_t bk = T::kSwap ? (uint64_t)((k / 4) * b_box16 + (k % 4) * kBStep)
+                                             : (uint64_t)(k * kBStep);
+                mma_f16_ss<T::kCG>(d_tmem, a_desc + k * kAStep, b_desc + bk, idesc, k > 0 ? 1u : acc);
+            }
             // stage free (in both CTAs of a pair) once these MMAs are done
             mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
             if (++s == S) {
@@ -367,6 +390,12 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
     const uint32_t lane_row = quarter * 32 + lane;  // TMEM lane = accumulator row
+    // swapped: the C column (within the tile) of this lane.  An M = 128 MMA
+    // puts accumulator row r in lane r; an M = 64 MMA (narrow tiles) puts it
+    // in lane (r / 16) * 32 + r % 16, leaving lanes 16..31 of each quarter
+    // unused (column past any tile).
+    const int32_t swap_col = pl.tile_n > 64 ? (int32_t)lane_row
+                                            : (lane < 16 ? (int32_t)(quarter * 16 + lane) : 1 << 30);
     const uint32_t half = T::kPair ? rank : 0u;      // which 128 rows of a pair tile
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
@@ -383,8 +412,8 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     // where chunk c of this thread's lane goes
     auto sink = [&](const WorkItem& it, uint32_t c) {
         if constexpr (T::kSwap) {
-            if (lane_row < (uint32_t)pl.tile_n)
-                sink_direct_swap(C, v, apply_relu, (int64_t)it.tn * pl.tile_n + lane_row,
+            if (swap_col < pl.tile_n)
+                sink_direct_swap(C, v, apply_relu, (int64_t)it.tn * pl.tile_n + swap_col,
                                  (int64_t)it.tm * pl.tile_m + c, M, N);
         } else {
             const int64_t row0 = (int64_t)it.tm * T::kTileM + 128 * half + 32 * quarter;
@@ -434,12 +463,37 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
         // so a warp writes / reads 512 contiguous bytes per instruction.
         if (cluster_split(pl)) {
             // Cluster split-K.  Each CTA holds one K range of this tile (its
-            // only item, so its ring is idle).  Ranks > 0 leave their fp32
-            // accumulator in their own ring, lane-interleaved float4 groups
-            // as for global partials, and signal rank 0; rank 0 adds them
-            // to its own in rank order, reading them over DSMEM.  The
-            // cluster barrier at teardown keeps the ranks alive until then.
+            // only item, so its ring is idle); rank 0 adds the other ranks'
+            // fp32 accumulators to its own in rank order.  Partials are
+            // lane-interleaved float4 groups as for global partials.
+            //   swapped (small partials): rank r > 0 pushes its partial
+            //     into slot r - 1 of rank 0's exchange buffer (behind the
+            //     ring; the plan reserves one slot, cluster = 2) with
+            //     asynchronous remote stores whose bytes complete rank 0's
+            //     exchange barrier; rank 0 reads them locally.
+            //   tiled: rank r > 0 leaves its partial in its own ring and
+            //     arrives on rank 0's barrier; rank 0 reads it over DSMEM.
+            // The cluster barrier at teardown keeps the ranks alive until
+            // rank 0 is done.
             const uint32_t exch = smem_u32(&ctrl->exch_bar);
+            const uint32_t slot_bytes = ncols * 128u * 4u;
+            if (T::kSwap && rank != 0) {
+                const uint32_t xbuf = mapa_shared(staging + (rank - 1u) * slot_bytes, 0);
+                const uint32_t xbar = mapa_shared(exch, 0);
+                for (uint32_t c = 0; c < ncols; c += kChunk) {
+                    __syncwarp();
+                    tmem_load_chunk<kMode>(taddr + c, v);
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j)
+                        st_async_v4_cluster(xbuf + (((c / 4 + j) * 128u + lane_row) << 4),
+                                            make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                                       __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])),
+                                            xbar);
+                }
+                release_tmem();
+                ++local;
+                continue;
+            }
             if (rank != 0) {
                 for (uint32_t c = 0; c < ncols; c += kChunk) {
                     __syncwarp();
@@ -481,8 +535,13 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
                 for (uint32_t r = 1; r < (uint32_t)pl.cluster; ++r) {
                     float4 x[kQ];
 #pragma unroll
-                    for (int j = 0; j < kQ; ++j)
-                        x[j] = ld_shared_cluster_f4(mapa_shared(stages + (((c / 4 + j) * 128u + lane_row) << 4), r));
+                    for (int j = 0; j < kQ; ++j) {
+                        const uint32_t off = ((c / 4 + j) * 128u + lane_row) << 4;
+                        if constexpr (T::kSwap)
+                            x[j] = ld_shared_f4(staging + (r - 1u) * slot_bytes + off);
+                        else
+                            x[j] = ld_shared_cluster_f4(mapa_shared(stages + off, r));
+                    }
 #pragma unroll
                     for (int j = 0; j < kQ; ++j) {
                         v[4 * j] += x[j].x;
@@ -611,12 +670,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = smem_u32(smem);
     const uint32_t stages = (base + (uint32_t)sizeof(Ctrl) + 1023u) & ~1023u;
     const gemm_relu_plan_t& pl = p.plan;
-    // MMA A operand per stage: two 64-wide chunks, or one for a narrow
-    // swapped tile (its second chunk then reads the next bytes of shared
-    // memory; those accumulator lanes are never stored)
-    const uint32_t a_bytes = (T::kSwap && pl.tile_n <= 64) ? kChunkBytes : kOperandA;
+    // MMA A operand per stage: 128 rows of 64 k; swapped, one 64-wide chunk
+    // of B columns (kBK k-rows) per 64 tile columns (a narrow tile, at most
+    // 64 columns, takes one chunk and an M = 64 MMA)
+    const uint32_t a_bytes = T::kSwap ? (pl.tile_n <= 64 ? 1u : 2u) * T::kBK * kSwizzleRow : kOperandA;
     const uint32_t b_bytes = (T::kPair ? T::kBCols * kBlockK * 2
-                                       : ((uint32_t)pl.mma_n * kBlockK * 2 + 1023u) & ~1023u);
+                                       : ((uint32_t)pl.mma_n * T::kBK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // CTA pairs (one MMA for two CTAs) and cluster split-K run in clusters
@@ -638,10 +697,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctrl->tmem_empty[b]), (T::kPair ? 2u : 1u) * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctrl->final_bar), 1);
-        mbar_init(smem_u32(&ctrl->exch_bar), pl.cluster > 1 ? (uint32_t)pl.cluster - 1u : 1u);
+        // cluster split-K: swapped, the peers push their partials into this
+        // CTA's buffer (one local arrival, completed by their bytes); tiled,
+        // each peer arrives once its partial sits in its own ring
+        mbar_init(smem_u32(&ctrl->exch_bar), (!T::kSwap && pl.cluster > 1) ? (uint32_t)pl.cluster - 1u : 1u);
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
         fence_mbar_init();
+        if (T::kSwap && cluster_split(pl) && rank == 0)
+            mbar_arrive_expect_tx(smem_u32(&ctrl->exch_bar),
+                                  ((uint32_t)pl.cluster - 1u) * (uint32_t)pl.mma_n * 128u * 4u);
     }
     if (warp == 1) {
         tmem_alloc<T::kCG>(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
@@ -684,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     if (clustered)
-        cluster_sync();  // a peer's shared memory may be read (MMA, DSMEM) until here
+        cluster_sync_relaxed();  // a peer's shared memory may be read (MMA, DSMEM) until here
     else
         __syncthreads();
     if (warp == 1) {

@@ -291,18 +291,23 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     }
     CUtensorMap ta, tb;
     const bool swap = (pl.path == 3);
+    // the swapped kernel's exchange buffer holds one peer's partial
+    if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
     int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u);
     if (rc != GEMM_OK) return rc;
-    // B: 64-column boxes (a narrow swapped tile: one box of tile_n columns)
+    // B: 64-column boxes of one stage's block_k k-rows (a narrow swapped
+    // tile: one box of tile_n columns)
     rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
-                   (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, kBlockK);
+                   (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k);
     if (rc != GEMM_OK) return rc;
     // C: 64-column x 32-row boxes, one per epilogue warp and chunk
     CUtensorMap tc;
     rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32);
     if (rc != GEMM_OK) return rc;
     if (swap) {
-        kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
+        // a narrow tile (<= 64 columns) runs M = 64 MMAs
+        kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/true,
+                                      /*b_mn=*/false);
         return launch_mode<2>(d, pl, kp, ta, tb, tc, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);

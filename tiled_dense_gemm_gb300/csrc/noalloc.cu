@@ -165,12 +165,13 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     kp.counters = reinterpret_cast<uint32_t*>(s.scratch + kCounterOffset);
     kp.ws = reinterpret_cast<float*>(s.scratch + kPartialOffset);
     kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
-    kp.idesc = make_idesc_f16_f32(128, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
+    kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/true,
+                                  /*b_mn=*/false);
 
     CUtensorMap ta, tb, tc;
     if ((rc = encode(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, (uint32_t)pl.tile_m)) != GEMM_OK) return rc;
     if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 64u,
-                     kBlockK)) != GEMM_OK)
+                     (uint32_t)pl.block_k)) != GEMM_OK)
         return rc;
     if ((rc = encode(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32)) != GEMM_OK) return rc;  // unused by this kernel
 

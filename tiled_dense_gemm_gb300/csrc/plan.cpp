@@ -15,9 +15,13 @@ constexpr int32_t kCtrlBytes = 1024;        // barriers + flags
 constexpr int32_t kAlignSlack = 1024;       // dynamic smem rounded up to 1 KiB
 constexpr int32_t kSmemLimit = 227 * 1024;  // opt-in shared memory per CTA
 constexpr int32_t kStagingBytes = 32 * 1024;  // C staging for TMA stores (tiled paths)
-constexpr int32_t kSwapStageBudget = kSmemLimit - kCtrlBytes - kAlignSlack;  // no C staging
 constexpr int32_t kMaxStages = 16;
+constexpr int32_t kSwizzleRowBytes = 128;   // one swizzled shared-memory row
 constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
+// k-rows per stage of the swapped-operand kernel: its MMAs are small
+// (N = padded M), so a stage of 128 k-rows halves the fixed per-stage cost
+// (barrier round trip, MMA commit, TMA issues) per byte streamed
+constexpr int32_t kSwapBlockK = 2 * kBlockK;
 
 // Cost model in microseconds, calibrated against GB300 measurements
 // (sm clock ~1.9-2.1 GHz): per-k-block mainloop time of each kernel shape,
@@ -148,28 +152,30 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     p.tiles_m = (int32_t)((M + p.tile_m - 1) / p.tile_m);
     p.tiles_n = (int32_t)((N + p.tile_n - 1) / p.tile_n);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.num_kb = (int32_t)((K + kBlockK - 1) / kBlockK);
+    p.block_k = (path == 3) ? kSwapBlockK : kBlockK;
+    p.num_kb = (int32_t)((K + p.block_k - 1) / p.block_k);
     p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
-    // per CTA: B columns it loads (half of the tile for a pair)
+    // per CTA: columns of the MMA B operand it loads (half of the tile for
+    // a pair; the padded rows of A when swapped)
     const int32_t b_cols = (path == 4) ? mma_n / 2 : mma_n;
-    const int32_t b_bytes = b_cols * kBlockK * 2;
-    // MMA A operand region per stage (a narrow swapped tile uses one chunk)
+    const int32_t b_bytes = b_cols * p.block_k * 2;
+    // MMA A operand per stage: 128 rows, or for the swapped kernel one
+    // 64-wide chunk of B columns per 64 tile columns (a narrow tile, at most
+    // 64 columns, takes one chunk and an M = 64 MMA)
     const bool narrow = (path == 3 && p.tile_n <= 64);
-    const int32_t a_region = narrow ? kOperandABytes / 2 : kOperandABytes;
-    // bytes the TMA copies of one stage deliver (boxes count in full)
-    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * kBlockK * 2 : kOperandABytes;
+    const int32_t a_region = (path == 3) ? (narrow ? 1 : 2) * p.block_k * kSwizzleRowBytes : kOperandABytes;
+    // bytes the TMA copies of one stage deliver
+    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * p.block_k * 2 : kOperandABytes;
     p.stage_bytes = a_box_bytes + b_bytes;
     const int32_t stride = a_region + ((b_bytes + 1023) / 1024) * 1024;
-    const int32_t staging = (path == 3) ? 0 : kStagingBytes;
-    // a narrow tile's unused second chunk of the last stage reads up to
-    // 8 KiB past the ring: keep that much shared memory behind it
-    const int32_t tail_pad = narrow ? kOperandABytes / 2 : 0;
-    const int32_t budget = (path == 3) ? kSwapStageBudget - tail_pad
-                                       : kSmemLimit - kCtrlBytes - kAlignSlack - staging;
+    // tiled paths: C staging for the TMA stores; swapped: the buffer a
+    // cluster split-K peer pushes its fp32 partial into (128 x mma_n)
+    const int32_t staging = (path == 3) ? 128 * mma_n * 4 : kStagingBytes;
+    const int32_t budget = kSmemLimit - kCtrlBytes - kAlignSlack - staging;
     int32_t stages = budget / stride;
     if (stages > kMaxStages) stages = kMaxStages;
     p.num_stages = stages;
-    p.smem_bytes = kCtrlBytes + kAlignSlack + stages * stride + staging + tail_pad;
+    p.smem_bytes = kCtrlBytes + kAlignSlack + stages * stride + staging;
     int32_t cols = 2 * mma_n;
     int32_t alloc = 32;
     while (alloc < cols) alloc *= 2;
@@ -273,6 +279,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     const char* f = force ? force : "";
     const bool dp_only = contains(f, ":dp");
     const bool force_csk = contains(f, ":c2");
+    const bool force_sk = contains(f, ":sk");
     int32_t force_splits = 0;
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 's' && q[2] >= '0' && q[2] <= '9') {
@@ -286,8 +293,10 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // A + B small enough to stay resident in the 126 MiB L2 next to C
     const bool operands_fit_l2 = 2.0 * ((double)M * K + (double)K * N) <= 48.0 * 1024 * 1024;
     // small M: the swapped-operand kernel (MMA N = padded M) for M <= 32;
-    // above that the 128 x 128 tiled kernel measured faster
-    bool want_swap = M <= 32, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
+    // for 32 < M <= 64 only where it splits K without stream-K (below);
+    // else, and above, the 128 x 128 tiled kernel measured faster
+    bool want_swap = M <= 64, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
+    const bool swap_only = M <= 32 || starts_with(f, "swap");
     if (starts_with(f, "swap") && M <= 128) {
         want_t256 = want_t128 = want_pair = false;
         want_swap = true;
@@ -308,6 +317,13 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         memset(&q, 0, sizeof(q));
         shape_plan(q, M, N, K, path, mma_n);
         double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2, pairs);
+        if (force_sk) {
+            // every tile stream-K over all workers
+            const int64_t units = (int64_t)q.num_tiles * q.num_kb;
+            q.cluster = (path == 4) ? 2 : 1;  // no cluster split-K
+            finish_split(q, (int32_t)(units < workers ? units : workers), 0, q.num_tiles);
+            cost = 0.0;
+        }
         if (force_csk && pairs > 0 && path != 4 && q.num_tiles <= pairs && q.num_kb >= 2) {
             finish_split(q, q.num_tiles, q.num_tiles, 0);
             q.cluster = 2;
@@ -358,14 +374,16 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
             *plan = q;
             return GEMM_OK;
         }
+        // (32 < M <= 64: only with >= 32 k-blocks; shorter K measured
+        // faster on the tiled kernel)
         if (force_splits <= 1 && !dp_only && !starts_with(f, "swap") && sp >= 2 && sp <= 4 &&
-            sp <= q.num_kb && 4 * q.num_tiles * sp >= 3 * num_sms) {
+            sp <= q.num_kb && 4 * q.num_tiles * sp >= 3 * num_sms && (M <= 32 || q.num_kb >= 32)) {
             finish_split(q, q.num_tiles * sp, 0, q.num_tiles, sp);
             q.grid = q.num_tiles * sp;
             *plan = q;
             return GEMM_OK;
         }
-        take(3, mpad, num_sms);
+        if (swap_only) take(3, mpad, num_sms);
     }
     if (want_pair) take(4, 256, pairs);
     if (want_t256) take(2, 256, num_sms);

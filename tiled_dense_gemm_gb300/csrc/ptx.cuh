@@ -64,6 +64,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// L2 policy that marks lines as the first to evict: for an operand that
+// every CTA together reads exactly once, so that it does not push reused
+// data out of L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// Either form, chosen per call.
+__device__ __forceinline__ void tma_load_2d_maybe_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                       int32_t x, int32_t y, bool hinted,
+                                                       uint64_t policy) {
+    if (hinted)
+        tma_load_2d_hint(dst, m, bar, x, y, policy);
+    else
+        tma_load_2d(dst, m, bar, x, y);
+}
+
 // 2-D tiled copy shared -> global (bulk-group completion).  Elements outside
 // the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x, int32_t y) {
@@ -116,6 +145,12 @@ __device__ __forceinline__ void cluster_sync() {
                      "memory");
 }
 
+// Execution-only cluster barrier: orders no memory operations, so it does
+// not wait for this thread's outstanding global stores.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Wait on a local mbarrier phase with acquire semantics at cluster scope
 // (arrivals came from other CTAs of the cluster).
 __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
@@ -136,6 +171,15 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
 }
 
 // 16-byte load from another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -143,6 +187,15 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory (both
+// addresses shared::cluster); its bytes complete the transaction count of
+// the mbarrier `bar` in that CTA.
+__device__ __forceinline__ void st_async_v4_cluster(uint32_t addr, uint4 v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+                 : "memory");
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (any CTA of
