@@ -65,6 +65,14 @@ def _load():
         lib.oracle_gemm_relu_entries.restype = ctypes.c_int
         lib.oracle_gemm_relu_entries.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int,
                                                  vp, vp, i64, vp, ctypes.c_int]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_gemm_relu_ex.restype = ctypes.c_int
+        lib.oracle_gemm_relu_ex.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, vp, vp, ctypes.c_int]
+        lib.oracle_gemm_relu_entries_ex.restype = ctypes.c_int
+        lib.oracle_gemm_relu_entries_ex.argtypes = [vp, vp, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, vp, vp, i64, vp, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         del dp
@@ -73,10 +81,12 @@ def _load():
 
 
 def _as_half_bits(x) -> np.ndarray:
-    """Accept float16 / uint16 numpy arrays or CPU torch fp16 tensors; return
-    a C-contiguous uint16 view of the raw binary16 bits."""
+    """Accept float16 / uint16 numpy arrays or CPU torch fp16 / bf16 tensors;
+    return a C-contiguous uint16 view of the raw 16-bit words."""
     if hasattr(x, "detach"):  # torch tensor
-        x = x.detach().cpu().contiguous().view(-1).numpy().view(np.uint16).reshape(tuple(x.shape))
+        import torch
+        t = x.detach().cpu().contiguous()
+        x = t.view(torch.int16).numpy().view(np.uint16).reshape(tuple(t.shape))
     x = np.ascontiguousarray(x)
     if x.dtype == np.float16:
         x = x.view(np.uint16)
@@ -138,6 +148,70 @@ def gemm_relu_entries(A, B, rows, cols, apply_relu: bool = True,
                                           cc.ctypes.data, r.size, out.ctypes.data, int(nt))
     if rc != 0:
         raise ValueError("oracle_gemm_relu_entries rejected its arguments")
+    return out
+
+
+# B layouts and element types of the _ex functions
+B_LAYOUTS = {"kn": 0, "nk": 1}
+DTYPES = {"f16": 0, "bf16": 1}
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().oracle_bf16_to_double(int(bits) & 0xFFFF))
+
+
+def gemm_relu_ex(A, B, apply_relu: bool = True, b_layout: str = "kn", dtype: str = "f16",
+                 threads: int | None = None) -> np.ndarray:
+    """C = ReLU(A.B) with B given as (K, N) ("kn") or as (N, K) ("nk", then
+    C = ReLU(A.B^T) of the stored matrix), elements binary16 ("f16") or
+    bfloat16 ("bf16") words.  Returns an (M, N) float64 array, unrounded."""
+    a = _as_half_bits(A)
+    b = _as_half_bits(B)
+    if a.ndim != 2 or b.ndim != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = a.shape
+    if b_layout == "kn":
+        K2, N = b.shape
+    elif b_layout == "nk":
+        N, K2 = b.shape
+    else:
+        raise ValueError(f"unknown B layout {b_layout!r}")
+    if K2 != K:
+        raise ValueError(f"shape mismatch {a.shape} . {b.shape} ({b_layout})")
+    c = np.empty((M, N), dtype=np.float64)
+    ad = np.empty(max(M * K, 1), dtype=np.float64)
+    bd = np.empty(max(K * N, 1), dtype=np.float64)
+    nt = threads if threads is not None else 1
+    rc = _load().oracle_gemm_relu_ex(a.ctypes.data, b.ctypes.data, c.ctypes.data, M, N, K,
+                                     int(bool(apply_relu)), B_LAYOUTS[b_layout], DTYPES[dtype],
+                                     ad.ctypes.data, bd.ctypes.data, int(nt))
+    if rc != 0:
+        raise ValueError("oracle_gemm_relu_ex rejected its arguments")
+    return c
+
+
+def gemm_relu_entries_ex(A, B, rows, cols, apply_relu: bool = True, b_layout: str = "kn",
+                         dtype: str = "f16", threads: int | None = None) -> np.ndarray:
+    """Entries (rows[t], cols[t]) of :func:`gemm_relu_ex`, each summed in k order."""
+    a = _as_half_bits(A)
+    b = _as_half_bits(B)
+    M, K = a.shape
+    N = b.shape[1] if b_layout == "kn" else b.shape[0]
+    K2 = b.shape[0] if b_layout == "kn" else b.shape[1]
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    cc = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != cc.shape:
+        raise ValueError("rows/cols length differ")
+    out = np.empty(r.shape, dtype=np.float64)
+    nt = threads if threads is not None else 1
+    rc = _load().oracle_gemm_relu_entries_ex(a.ctypes.data, b.ctypes.data, M, N, K,
+                                             int(bool(apply_relu)), B_LAYOUTS[b_layout],
+                                             DTYPES[dtype], r.ctypes.data, cc.ctypes.data, r.size,
+                                             out.ctypes.data, int(nt))
+    if rc != 0:
+        raise ValueError("oracle_gemm_relu_entries_ex rejected its arguments")
     return out
 
 

@@ -10,7 +10,8 @@ mistakes they are meant to catch.
 What fixes the expected values, none of it the oracle's own code:
 * hand-worked fixtures (tests/golden), exact rationals;
 * brute force in exact rational arithmetic (``fractions``) on tiny inputs,
-  with binary16 values decoded by numpy;
+  with binary16 values decoded by numpy (bfloat16 words by a float32 bit
+  shift);
 * integer inputs whose products and sums are exact in every format,
   checked against numpy int64 matmul;
 * closed forms: identity B gives ReLU(A), all-ones A gives ReLU of B's
@@ -32,8 +33,37 @@ from golden_io import all_fixtures
 U64 = 2.0 ** -53  # unit roundoff of binary64
 
 
+class F16:
+    """binary16 inputs: numpy float16 arrays, decoded by numpy."""
+    name = "f16"
+
+    @staticmethod
+    def enc(x):
+        return np.asarray(x, dtype=np.float64).astype(np.float16)
+
+    @staticmethod
+    def dec(a):
+        return np.asarray(a).astype(np.float64)
+
+
+class BF16:
+    """bfloat16 inputs: uint16 words (the top half of a binary32), decoded by
+    shifting them into a numpy float32 -- not by the oracle's decoder."""
+    name = "bf16"
+
+    @staticmethod
+    def enc(x):
+        f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+        u = f.view(np.uint32).astype(np.uint64)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)  # round to nearest even
+
+    @staticmethod
+    def dec(a):
+        return (np.ascontiguousarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
 def _h(x):
-    return np.asarray(x, dtype=np.float64).astype(np.float16)
+    return F16.enc(x)
 
 
 def _frac(x):
@@ -42,21 +72,21 @@ def _frac(x):
     return Fraction(x) if np.isfinite(x) else None
 
 
-def _exact_product(A16, B16):
-    """Exact rational A.B (lists of Fractions) from binary16 inputs."""
-    Af = [[Fraction(float(v)) for v in row] for row in A16.astype(np.float64)]
-    Bf = [[Fraction(float(v)) for v in row] for row in B16.astype(np.float64)]
+def _exact_product(A16, B16, fmt=F16):
+    """Exact rational A.B (lists of Fractions) from 16-bit inputs."""
+    Af = [[Fraction(float(v)) for v in row] for row in fmt.dec(A16)]
+    Bf = [[Fraction(float(v)) for v in row] for row in fmt.dec(B16)]
     M, K = len(Af), len(Bf)
     N = B16.shape[1]
     return [[sum((Af[i][k] * Bf[k][j] for k in range(K)), Fraction(0)) for j in range(N)]
             for i in range(M)]
 
 
-def _bound(A16, B16):
+def _bound(A16, B16, fmt=F16):
     """gamma_K * |A|.|B| : a rigorous bound on binary64 accumulation error."""
     K = A16.shape[1]
     gk = K * U64 / (1 - K * U64) if K else 0.0
-    return gk * (np.abs(A16.astype(np.float64)) @ np.abs(B16.astype(np.float64)))
+    return gk * (np.abs(fmt.dec(A16)) @ np.abs(fmt.dec(B16)))
 
 
 def pin_golden(ref):
@@ -72,15 +102,15 @@ def pin_golden(ref):
     return fails
 
 
-def pin_bruteforce(ref, trials=40, seed=123):
+def pin_bruteforce(ref, trials=40, seed=123, fmt=F16):
     rng = np.random.default_rng(seed)
     fails = []
     for t in range(trials):
         M, N, K = (int(x) for x in rng.integers(1, 8, size=3))
-        A = _h(rng.standard_normal((M, K)) * 3)
-        B = _h(rng.standard_normal((K, N)) * 3)
-        exact = _exact_product(A, B)
-        bnd = _bound(A, B)
+        A = fmt.enc(rng.standard_normal((M, K)) * 3)
+        B = fmt.enc(rng.standard_normal((K, N)) * 3)
+        exact = _exact_product(A, B, fmt)
+        bnd = _bound(A, B, fmt)
         for relu in (True, False):
             got = ref(A, B, relu)
             for i in range(M):
@@ -95,7 +125,7 @@ def pin_bruteforce(ref, trials=40, seed=123):
     return fails
 
 
-def pin_integer_exact(ref, seed=7):
+def pin_integer_exact(ref, seed=7, fmt=F16):
     rng = np.random.default_rng(seed)
     M, N, K = 33, 47, 300
     Ai = rng.integers(-2, 3, size=(M, K))
@@ -103,7 +133,7 @@ def pin_integer_exact(ref, seed=7):
     exact = Ai.astype(np.int64) @ Bi.astype(np.int64)
     fails = []
     for relu in (True, False):
-        got = ref(_h(Ai), _h(Bi), relu)
+        got = ref(fmt.enc(Ai), fmt.enc(Bi), relu)
         exp = np.maximum(exact, 0) if relu else exact
         if not np.array_equal(got, exp.astype(np.float64)):
             bad = np.argwhere(got != exp)
@@ -111,25 +141,26 @@ def pin_integer_exact(ref, seed=7):
     return fails
 
 
-def pin_identity(ref, seed=11):
+def pin_identity(ref, seed=11, fmt=F16):
     rng = np.random.default_rng(seed)
     M, K = 9, 13
-    A = _h(rng.standard_normal((M, K)))
-    I = _h(np.eye(K))
+    A = fmt.enc(rng.standard_normal((M, K)))
+    I = fmt.enc(np.eye(K))
     got = ref(A, I, True)
-    exp = np.maximum(A.astype(np.float64), 0.0)
+    exp = np.maximum(fmt.dec(A), 0.0)
     return [] if np.array_equal(got, exp) else ["identity B did not give ReLU(A)"]
 
 
-def pin_ones(ref, seed=12):
+def pin_ones(ref, seed=12, fmt=F16):
     rng = np.random.default_rng(seed)
     M, N, K = 4, 10, 12
     Ai = np.ones((M, K))
-    B = _h(rng.standard_normal((K, N)))
+    B = fmt.enc(rng.standard_normal((K, N)))
+    Bv = fmt.dec(B)
     fails = []
-    colsum = [sum((Fraction(float(B[k, j])) for k in range(K)), Fraction(0)) for j in range(N)]
-    bnd = _bound(_h(Ai), B)
-    got = ref(_h(Ai), B, True)
+    colsum = [sum((Fraction(float(Bv[k, j])) for k in range(K)), Fraction(0)) for j in range(N)]
+    bnd = _bound(fmt.enc(Ai), B, fmt)
+    got = ref(fmt.enc(Ai), B, True)
     for i in range(M):
         for j in range(N):
             e = max(colsum[j], Fraction(0))
@@ -139,12 +170,12 @@ def pin_ones(ref, seed=12):
     return fails
 
 
-def pin_invariants(ref, seed=13):
+def pin_invariants(ref, seed=13, fmt=F16):
     rng = np.random.default_rng(seed)
     fails = []
     M, N, K = 17, 23, 29
-    A = _h(rng.standard_normal((M, K)))
-    B = _h(rng.standard_normal((K, N)))
+    A = fmt.enc(rng.standard_normal((M, K)))
+    B = fmt.enc(rng.standard_normal((K, N)))
     on = ref(A, B, True)
     off = ref(A, B, False)
     if (on < 0).any() or np.signbit(on).any():
@@ -152,14 +183,14 @@ def pin_invariants(ref, seed=13):
     if not np.array_equal(on, np.where(off > 0, off, 0.0)):
         fails.append("relu-on != max(relu-off, 0)")
     # zero K padding
-    Ap = np.concatenate([A, np.zeros((M, 7), np.float16)], axis=1)
-    Bp = np.concatenate([B, np.zeros((7, N), np.float16)], axis=0)
+    Ap = np.concatenate([A, fmt.enc(np.zeros((M, 7)))], axis=1)
+    Bp = np.concatenate([B, fmt.enc(np.zeros((7, N)))], axis=0)
     if not np.array_equal(ref(Ap, Bp, False), off):
         fails.append("zero K-tail changed the result")
-    # odd in A, homogeneous in B (scaling by 2 is exact in both formats)
-    if not np.array_equal(ref(-A, B, False), -off):
+    # odd in A, homogeneous in B (negation and scaling by 2 are exact)
+    if not np.array_equal(ref(fmt.enc(-fmt.dec(A)), B, False), -off):
         fails.append("relu-off not odd in A")
-    if not np.array_equal(ref(A, _h(B.astype(np.float64) * 2), False), 2 * off):
+    if not np.array_equal(ref(A, fmt.enc(fmt.dec(B) * 2), False), 2 * off):
         fails.append("relu-off not homogeneous in B")
     # transpose: (A.B)^T == B^T.A^T (same k order per entry => bit-identical)
     if not np.array_equal(ref(np.ascontiguousarray(B.T), np.ascontiguousarray(A.T), False), off.T):
@@ -167,13 +198,13 @@ def pin_invariants(ref, seed=13):
     return fails
 
 
-def pin_torch64(ref, seed=14):
+def pin_torch64(ref, seed=14, fmt=F16):
     rng = np.random.default_rng(seed)
     M, N, K = 40, 50, 300
-    A = _h(rng.standard_normal((M, K)))
-    B = _h(rng.standard_normal((K, N)))
-    lib = (torch.from_numpy(A.astype(np.float64)) @ torch.from_numpy(B.astype(np.float64))).numpy()
-    bnd = 2 * _bound(A, B)  # both sides round in binary64, orders may differ
+    A = fmt.enc(rng.standard_normal((M, K)))
+    B = fmt.enc(rng.standard_normal((K, N)))
+    lib = (torch.from_numpy(fmt.dec(A)) @ torch.from_numpy(fmt.dec(B))).numpy()
+    bnd = 2 * _bound(A, B, fmt)  # both sides round in binary64, orders may differ
     fails = []
     for relu in (True, False):
         exp = np.maximum(lib, 0) if relu else lib
@@ -186,3 +217,6 @@ def pin_torch64(ref, seed=14):
 
 ALL_PINS = [pin_golden, pin_bruteforce, pin_integer_exact, pin_identity, pin_ones,
             pin_invariants, pin_torch64]
+# the pins that take a ``fmt`` (the golden fixtures are binary16 values)
+FMT_PINS = [pin_bruteforce, pin_integer_exact, pin_identity, pin_ones, pin_invariants,
+            pin_torch64]

@@ -128,3 +128,93 @@ def test_pins_catch_planted_mistake(oracle_mod, idx):
     mutant = _mutants(oracle_mod)[idx]
     caught = [pin.__name__ for pin in P.ALL_PINS if pin(mutant)]
     assert caught, f"no pin caught the planted mistake {mutant.__name__}"
+
+
+# ---- B stored (N, K) and bfloat16 elements (oracle_gemm_relu_ex) -----------
+
+def test_bf16_decode_matches_float32_top_half(oracle_mod):
+    # a bfloat16 word is the top half of a binary32: decode by shifting
+    known = {0x3F80: 1.0, 0xC040: -3.0, 0x7F7F: 3.3895313892515355e38, 0x0001: 2.0 ** -133,
+             0x0080: 2.0 ** -126, 0x3EAB: 0.333984375, 0x7F80: float("inf")}
+    for bits, val in known.items():
+        assert oracle_mod.bf16_to_double(bits) == val, hex(bits)
+    assert np.signbit(oracle_mod.bf16_to_double(0x8000))
+    assert np.isnan(oracle_mod.bf16_to_double(0x7FC0))
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = P.BF16.dec(bits)
+    got = np.array([oracle_mod.bf16_to_double(int(b)) for b in bits])
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.signbit(got[finite]), np.signbit(ref[finite]))
+
+
+def _ex_ref(oracle_mod, layout, dtype):
+    """ref(A, B_kn, relu) through gemm_relu_ex; for "nk" the (K, N) operand of
+    the pins is stored transposed, as an (N, K) row-major matrix."""
+    def ref(A, B, relu):
+        Bs = np.ascontiguousarray(B.T) if layout == "nk" else B
+        return oracle_mod.gemm_relu_ex(A, Bs, relu, b_layout=layout, dtype=dtype)
+    return ref
+
+
+FMTS = {"f16": P.F16, "bf16": P.BF16}
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("pin", P.FMT_PINS, ids=lambda f: f.__name__)
+def test_ex_oracle_passes_pin(oracle_mod, layout, dtype, pin):
+    fails = pin(_ex_ref(oracle_mod, layout, dtype), fmt=FMTS[dtype])
+    assert not fails, "\n".join(fails[:10])
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_ex_f16_passes_golden(oracle_mod, layout):
+    fails = P.pin_golden(_ex_ref(oracle_mod, layout, "f16"))
+    assert not fails, "\n".join(fails[:10])
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_ex_layouts_agree_bit_for_bit(oracle_mod, dtype):
+    rng = np.random.default_rng(21)
+    fmt = FMTS[dtype]
+    A = fmt.enc(rng.standard_normal((29, 75)))
+    B = fmt.enc(rng.standard_normal((75, 43)))
+    kn = oracle_mod.gemm_relu_ex(A, B, True, "kn", dtype)
+    nk = oracle_mod.gemm_relu_ex(A, np.ascontiguousarray(B.T), True, "nk", dtype)
+    assert np.array_equal(kn, nk)
+    if dtype == "f16":
+        assert np.array_equal(kn, oracle_mod.gemm_relu(A, B, True))
+    rows = rng.integers(0, 29, 50)
+    cols = rng.integers(0, 43, 50)
+    ent = oracle_mod.gemm_relu_entries_ex(A, np.ascontiguousarray(B.T), rows, cols, True, "nk", dtype)
+    assert np.array_equal(ent, kn[rows, cols])
+
+
+def _ex_mutants(oracle_mod):
+    ex = oracle_mod.gemm_relu_ex
+
+    def bf16_read_as_f16(A, B, r):  # element type ignored
+        return ex(A, np.ascontiguousarray(B.T), r, "nk", "f16")
+
+    def nk_read_with_kn_strides(A, B, r):  # layout ignored: (N, K) storage walked as (K, N)
+        Bs = np.ascontiguousarray(B.T)
+        return ex(A, Bs.reshape(B.shape), r, "kn", "bf16")
+
+    def bf16_exponent_off_by_one(A, B, r):
+        return ex(A, np.ascontiguousarray(B.T), r, "nk", "bf16") * 2.0
+
+    def nk_last_k_dropped(A, B, r):
+        if A.shape[1] <= 1:
+            return np.zeros((A.shape[0], B.shape[1]))
+        Bs = np.ascontiguousarray(B.T[:, :-1])
+        return ex(np.ascontiguousarray(A[:, :-1]), Bs, r, "nk", "bf16")
+
+    return [bf16_read_as_f16, nk_read_with_kn_strides, bf16_exponent_off_by_one, nk_last_k_dropped]
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_fmt_pins_catch_planted_mistake_in_ex(oracle_mod, idx):
+    mutant = _ex_mutants(oracle_mod)[idx]
+    caught = [pin.__name__ for pin in P.FMT_PINS if pin(mutant, fmt=P.BF16)]
+    assert caught, f"no pin caught the planted mistake {mutant.__name__}"
