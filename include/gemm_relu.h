@@ -66,6 +66,36 @@ typedef enum {
 int gemm_relu(const void* A, const void* B, void* C,
               int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);
 
+/* Layouts of B for gemm_relu_ex. */
+typedef enum {
+    GEMM_B_KN = 0, /* B is K x N row-major (leading dimension N): C = ReLU(A . B) */
+    GEMM_B_NK = 1  /* B is N x K row-major (leading dimension K): C = ReLU(A . B^T) */
+} gemm_b_layout_t;
+
+/* Element types of A, B and C for gemm_relu_ex (accumulation is fp32). */
+typedef enum {
+    GEMM_DTYPE_F16 = 0,  /* IEEE binary16 */
+    GEMM_DTYPE_BF16 = 1  /* bfloat16 */
+} gemm_dtype_t;
+
+/*
+ * gemm_relu with a choice of B layout and element type.  The (N, K) form of
+ * B is the GEMM of "TileLang Guide: Composable Tiled AI Kernel Programming"
+ * (sections "Tiles as First-Class Language Primitives" and "Production
+ * Implementation", Step 1: B buffer (N, K), tile product with transpose_B);
+ * bfloat16 is the element type of that page's FlashMLA listing.
+ *
+ * A (M x K) and C (M x N) are row-major; B is laid out as `b_layout` says;
+ * all three hold `dtype` elements, and C is rounded to nearest-even in that
+ * type.  Every other rule is gemm_relu's: 16-byte aligned pointers, K % 8 ==
+ * 0 and N % 8 == 0, asynchronous on `stream`, the same workspace.
+ * gemm_relu(...) is gemm_relu_ex(..., GEMM_B_KN, GEMM_DTYPE_F16, stream).
+ * An unknown b_layout or dtype returns GEMM_ERR_INVALID_ARG.
+ */
+int gemm_relu_ex(const void* A, const void* B, void* C,
+                 int64_t M, int64_t N, int64_t K, int apply_relu,
+                 int b_layout, int dtype, void* stream);
+
 /*
  * Same operation on HOST buffers: copies A and B to library-owned device
  * buffers (one cudaMemcpyAsync each), runs gemm_relu on `stream`, copies C

@@ -85,3 +85,35 @@ def test_python_wrapper_rejects_bad_tensors(gemm_lib):
         gemm_lib.gemm_relu(a.float(), b)
     with pytest.raises(ValueError):
         gemm_lib.gemm_relu(a, torch.zeros(4, 8, dtype=torch.float16))
+
+
+def test_ex_entry_point_checks(gemm_lib):
+    L = gemm_lib.lib()
+    good = 4096
+    ex = lambda *a: L.gemm_relu_ex(*a, None)  # noqa: E731
+    # unknown layout / element type
+    assert ex(good, good, good, 8, 8, 8, 1, 2, 0) == 1
+    assert ex(good, good, good, 8, 8, 8, 1, -1, 0) == 1
+    assert ex(good, good, good, 8, 8, 8, 1, 0, 2) == 1
+    # gemm_relu's own checks apply to every layout and type
+    for layout in (0, 1):
+        for dtype in (0, 1):
+            assert ex(good, good, good, -1, 8, 8, 1, layout, dtype) == 1
+            assert ex(good, good, good, 8, 8, 12, 1, layout, dtype) == 2
+            assert ex(good, good, good, 8, 12, 8, 1, layout, dtype) == 2
+            assert ex(good, good + 8, good, 8, 8, 8, 1, layout, dtype) == 2
+            assert ex(None, None, None, 0, 8, 8, 1, layout, dtype) == 0
+            if not torch.cuda.is_available():
+                assert ex(good, good, good, 8, 8, 8, 1, layout, dtype) == 3
+
+
+def test_ex_python_wrapper_rejects_bad_tensors(gemm_lib):
+    a = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        gemm_lib.gemm_relu_ex(a, torch.zeros(8, 8, dtype=torch.float16))  # mixed types
+    with pytest.raises(ValueError):
+        gemm_lib.gemm_relu_ex(a, torch.zeros(8, 8, dtype=torch.bfloat16), b_layout="tn")
+    with pytest.raises(ValueError):
+        gemm_lib.gemm_relu_ex(a, torch.zeros(6, 4, dtype=torch.bfloat16), b_layout="nk")  # K differs
+    with pytest.raises(ValueError):
+        gemm_lib.gemm_relu_ex(a, torch.zeros(16, 8, dtype=torch.bfloat16), b_layout="nk")  # CPU

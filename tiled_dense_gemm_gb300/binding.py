@@ -65,6 +65,8 @@ def lib():
         i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         L.gemm_relu.restype = i32
         L.gemm_relu.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_ex.restype = i32
+        L.gemm_relu_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, i32, vp]
         L.gemm_relu_host.restype = i32
         L.gemm_relu_host.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
         L.gemm_relu_noalloc.restype = i32
@@ -148,6 +150,45 @@ def gemm_relu(a, b, c=None, apply_relu: bool = True, stream=None):
                              int(bool(apply_relu)), _stream_handle(stream, a.device))
     if rc != GEMM_OK:
         raise GemmReluError(rc, "gemm_relu")
+    return c
+
+
+B_LAYOUTS = {"kn": 0, "nk": 1}  # gemm_b_layout_t
+
+
+def gemm_relu_ex(a, b, c=None, apply_relu: bool = True, b_layout: str = "kn", stream=None):
+    """C = ReLU(a @ b) for b_layout "kn" (b is (K, N)) or ReLU(a @ b.T) for
+    "nk" (b is (N, K)); a, b and c are CUDA tensors of one element type,
+    float16 or bfloat16.  ``c`` (M, N) is written in place when given."""
+    import torch
+    if not (isinstance(a, torch.Tensor) and isinstance(b, torch.Tensor)):
+        raise TypeError("a and b must be torch tensors")
+    dtypes = {torch.float16: 0, torch.bfloat16: 1}
+    if a.dtype not in dtypes or b.dtype != a.dtype:
+        raise TypeError("a and b must both be float16 or both bfloat16")
+    if b_layout not in B_LAYOUTS:
+        raise ValueError(f"b_layout must be 'kn' or 'nk', not {b_layout!r}")
+    if a.dim() != 2 or b.dim() != 2:
+        raise ValueError("a and b must be 2-D")
+    M, K = a.shape
+    N, Kb = (b.shape[1], b.shape[0]) if b_layout == "kn" else (b.shape[0], b.shape[1])
+    if Kb != K:
+        raise ValueError(f"bad shapes {tuple(a.shape)} and {tuple(b.shape)} ({b_layout})")
+    if not (a.is_cuda and b.is_cuda) or a.device != b.device:
+        raise ValueError("a and b must be CUDA tensors on the same device")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous row-major (call .contiguous())")
+    if c is None:
+        c = torch.empty((M, N), dtype=a.dtype, device=a.device)
+    elif (c.dtype != a.dtype or tuple(c.shape) != (M, N) or c.device != a.device
+          or not c.is_contiguous()):
+        raise ValueError("c must be a contiguous (M, N) tensor of a's type on a's device")
+    with torch.cuda.device(a.device):
+        rc = lib().gemm_relu_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                                int(bool(apply_relu)), B_LAYOUTS[b_layout], dtypes[a.dtype],
+                                _stream_handle(stream, a.device))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu_ex")
     return c
 
 

@@ -6,12 +6,16 @@
 //               ring of shared-memory stages (128-byte swizzle), each stage
 //               guarded by a full/empty mbarrier pair;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (fp16 x fp16 -> fp32, 128 x N x 16 per instruction) into one
+//               (fp16 or bf16 inputs -> fp32, 128 x N x 16 per instruction) into one
 //               of two TMEM accumulators and commits stage releases;
 //   warps 2-5   epilogue: TMEM -> registers (each warp owns a 32-lane
-//               quarter of the accumulator), ReLU, round to fp16, store to
+//               quarter of the accumulator), ReLU, round to fp16/bf16, store to
 //               C; or, for a tile split along K, store an fp32 partial and
 //               let the last CTA to finish sum the partials in slot order.
+// B is read as stored: (K, N) row-major (an MN-major MMA operand) or
+// (N, K) row-major (K-major, C = ReLU(A . B^T)); the layout and the element
+// type are runtime flags that change only descriptors, copy coordinates and
+// the final rounding.
 // The two accumulators let the epilogue of tile i overlap the mainloop of
 // tile i+1.  Every wait is bounded: on timeout the CTA records an error
 // word, tells its other roles to stop, lets in-flight copies and MMAs land,
@@ -26,6 +30,7 @@
 // tile.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -68,9 +73,11 @@ struct KParams {
     gemm_relu_plan_t plan;
     int64_t M, N, K;
     int32_t apply_relu;
+    int32_t b_kmajor;     // B stored (N, K) row-major (C = ReLU(A . B^T)) instead of (K, N)
+    int32_t out_bf16;     // elements are bfloat16 (inputs and C) instead of binary16
     uint32_t idesc;
     uint64_t timeout_ns;
-    __half* C;
+    uint16_t* C;          // 16-bit words of C (binary16 or bfloat16)
     float* ws;            // stream-K partial tiles: [sk_tile][slot][col][128 lanes]
     uint32_t* counters;   // stream-K arrivals, one per stream-K tile, zero between launches
     int32_t* err;         // first error code of the launch (0 = none)
@@ -126,9 +133,19 @@ __device__ __forceinline__ float relu_if(float x, int32_t apply) {
     return apply ? (x > 0.0f ? x : 0.0f) : x;
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+// Two fp32 values rounded to nearest-even 16-bit floats, a in the low half.
+__device__ __forceinline__ uint32_t pack2(float a, float b, int32_t bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t round16(float x, int32_t bf16) {
+    if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    return __half_as_ushort(__float2half_rn(x));
 }
 
 // ------------------------------------------------------------------ roles
@@ -163,6 +180,8 @@ struct Producer {
     bool once_a, once_b;
     uint64_t pol_first;
     uint32_t a_sub_bytes;  // swapped: bytes of one 64-k box of A's padded rows
+    bool b_nk;             // B stored (N, K): its boxes are (64 k) x (rows of N)
+    uint32_t b_sub_bytes;  // swapped, B stored (N, K): bytes of one 64-k box of the tile's B rows
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
@@ -176,6 +195,8 @@ struct Producer {
         // expects the bytes of both CTAs
         tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
         a_sub_bytes = (uint32_t)pl.tile_m * kSwizzleRow;
+        b_nk = p_.b_kmajor != 0;
+        b_sub_bytes = (pl.tile_n <= 64 ? 64u : 128u) * kSwizzleRow;
         once_a = pl.tiles_n == 1;
         once_b = pl.tiles_m == 1;
         pol_first = l2_policy_evict_first();
@@ -211,25 +232,44 @@ struct Producer {
                 const uint32_t full_leader = mapa_shared(full, 0);
                 if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
                 tma_load_2d_pair(a_dst, tmA, full_leader, k0, a_row);
+                if (b_nk) {
+                    tma_load_2d_pair(b_dst, tmB, full_leader, k0, b_col);  // this CTA's 128 rows of B
+                } else {
 #pragma unroll
-                for (uint32_t j = 0; j < T::kBCols / 64; ++j)
-                    tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                    for (uint32_t j = 0; j < T::kBCols / 64; ++j)
+                        tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                }
             } else {
                 mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
                     tma_load_2d_maybe_hint(a_dst, tmA, full, k0, a_row, once_a, pol_first);
+                    if (b_nk) {
+                        // the tile's kBN rows of B, K-major like A
+                        tma_load_2d_maybe_hint(b_dst, tmB, full, k0, b_col, once_b, pol_first);
+                    } else {
 #pragma unroll
-                    for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                        tma_load_2d_maybe_hint(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0,
-                                               once_b, pol_first);
+                        for (uint32_t j = 0; j < T::kBN / 64; ++j)
+                            tma_load_2d_maybe_hint(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0,
+                                                   once_b, pol_first);
+                    }
                 } else {
                     // MMA A operand: the tile's columns of B, one 64-wide chunk
                     // of kBK k-rows per TMA box (a narrow tile fills part of
                     // one chunk)
                     constexpr uint32_t kSwapChunk = T::kBK * kSwizzleRow;
-                    tma_load_2d_maybe_hint(a_dst, tmB, full, b_col, k0, once_b, pol_first);
-                    if (pl.tile_n > 64)
-                        tma_load_2d_maybe_hint(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b, pol_first);
+                    if (b_nk) {
+                        // B stored (N, K): the tile's B rows, one K-major box
+                        // per 64 k
+#pragma unroll
+                        for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
+                            tma_load_2d_maybe_hint(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK),
+                                                   b_col, once_b, pol_first);
+                    } else {
+                        tma_load_2d_maybe_hint(a_dst, tmB, full, b_col, k0, once_b, pol_first);
+                        if (pl.tile_n > 64)
+                            tma_load_2d_maybe_hint(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b,
+                                                   pol_first);
+                    }
                     // MMA B operand: the (padded) rows of A, one box per 64 k
 #pragma unroll
                     for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
@@ -261,18 +301,39 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     const uint32_t empty0 = smem_u32(&ctrl->empty[0]);
     const uint32_t tfull0 = smem_u32(&ctrl->tmem_full[0]);
     const uint32_t tempty0 = smem_u32(&ctrl->tmem_empty[0]);
-    // Descriptors of stage 0 and per-16-k advances, in 16-byte units.
-    // K-major operand (A; A^T when swapped): +32 bytes inside the swizzled
-    // row.  MN-major operand (B; B^T when swapped): +16 k-rows = 2 atoms.
-    // Swapped: the B^T chunks are kBK k-rows long; A^T is one 64-k box of
-    // the padded rows per 64 k, so its k16 step also hops boxes.
-    const uint64_t a_desc0 = T::kSwap ? make_sw128_desc(stages, T::kBK * kSwizzleRow, kAtomBytes)
-                                      : make_sw128_desc(stages, 16, kAtomBytes);
-    const uint64_t b_desc0 = T::kSwap ? make_sw128_desc(stages + a_bytes, 16, kAtomBytes)
-                                      : make_sw128_desc(stages + a_bytes, kChunkBytes, kAtomBytes);
-    constexpr uint32_t kAStep = (T::kSwap ? 2 * kAtomBytes : 32u) >> 4;
-    constexpr uint32_t kBStep = (T::kSwap ? 32u : 2 * kAtomBytes) >> 4;
-    const uint32_t b_box16 = ((uint32_t)pl.tile_m * kSwizzleRow) >> 4;  // swapped: one 64-k box of A
+    // Descriptors of stage 0 and, per MMA of a stage, the offset (16-byte
+    // units) of each operand's k16 slice:
+    //   K-major operand (A; B stored (N, K); when swapped A^T, and B^T of a
+    //     B stored (N, K)): +32 bytes inside the swizzled row, and one box
+    //     of rows further per 64 k;
+    //   MN-major operand (B stored (K, N); B^T of it when swapped): +16
+    //     k-rows (2 atoms); its 64-wide chunks are LBO apart.
+    constexpr uint32_t kK = T::kBK / 16;  // MMAs per stage
+    constexpr uint32_t kMNStep = (2 * kAtomBytes) >> 4;
+    const bool b_nk = p.b_kmajor != 0;
+    uint64_t a_desc0, b_desc0;
+    uint32_t a_off[kK], b_off[kK];
+    if constexpr (T::kSwap) {
+        const uint32_t a_box16 = ((pl.tile_n <= 64 ? 64u : 128u) * kSwizzleRow) >> 4;
+        const uint32_t b_box16 = ((uint32_t)pl.tile_m * kSwizzleRow) >> 4;  // one 64-k box of A's rows
+        a_desc0 = b_nk ? make_sw128_desc(stages, 16, kAtomBytes)
+                       : make_sw128_desc(stages, T::kBK * kSwizzleRow, kAtomBytes);
+        b_desc0 = make_sw128_desc(stages + a_bytes, 16, kAtomBytes);
+#pragma unroll
+        for (uint32_t k = 0; k < kK; ++k) {
+            a_off[k] = b_nk ? (k / 4) * a_box16 + (k % 4) * 2u : k * kMNStep;
+            b_off[k] = (k / 4) * b_box16 + (k % 4) * 2u;
+        }
+    } else {
+        a_desc0 = make_sw128_desc(stages, 16, kAtomBytes);
+        b_desc0 = b_nk ? make_sw128_desc(stages + a_bytes, 16, kAtomBytes)
+                       : make_sw128_desc(stages + a_bytes, kChunkBytes, kAtomBytes);
+#pragma unroll
+        for (uint32_t k = 0; k < kK; ++k) {
+            a_off[k] = k * 2u;
+            b_off[k] = b_nk ? k * 2u : k * kMNStep;
+        }
+    }
     const uint32_t stride16 = stride >> 4;
     WorkIter wi;
     wi.init(pl, worker, (int32_t)rank);
@@ -291,11 +352,8 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
             const uint64_t b_desc = b_desc0 + (uint64_t)(s * stride16);
             const uint32_t acc = (kb > w.kb0) ? 1u : 0u;
 #pragma unroll
-            for (uint32_t k = 0; k < T::kBK / 16; ++k) {
-                const uint64_t bk = T::kSwap ? (uint64_t)((k / 4) * b_box16 + (k % 4) * kBStep)
-                                             : (uint64_t)(k * kBStep);
-                mma_f16_ss<T::kCG>(d_tmem, a_desc + k * kAStep, b_desc + bk, idesc, k > 0 ? 1u : acc);
-            }
+            for (uint32_t k = 0; k < kK; ++k)
+                mma_f16_ss<T::kCG>(d_tmem, a_desc + a_off[k], b_desc + b_off[k], idesc, k > 0 ? 1u : acc);
             // stage free (in both CTAs of a pair) once these MMAs are done
             mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
             if (++s == S) {
@@ -334,8 +392,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 q) {
 // Tiled / pair paths: one 64-column chunk of this warp's 32 rows -> C.
 // `lane` is the row within the warp's slab; `sbuf` alternates buffers.
 __device__ __forceinline__ void sink_tma(const CUtensorMap* tmC, uint32_t stage_buf, uint32_t lane,
-                                         const float* v, int32_t apply_relu, int64_t col, int64_t row0,
-                                         int64_t M, int64_t N) {
+                                         const float* v, int32_t apply_relu, int32_t bf16, int64_t col,
+                                         int64_t row0, int64_t M, int64_t N) {
     // the copy issued two chunks ago from this buffer must have read it
     if (lane == 0) bulk_wait_group_read<1>();
     __syncwarp();
@@ -343,10 +401,10 @@ __device__ __forceinline__ void sink_tma(const CUtensorMap* tmC, uint32_t stage_
 #pragma unroll
     for (uint32_t u = 0; u < 8; ++u) {
         uint4 q;
-        q.x = pack_half2(relu_if(v[8 * u + 0], apply_relu), relu_if(v[8 * u + 1], apply_relu));
-        q.y = pack_half2(relu_if(v[8 * u + 2], apply_relu), relu_if(v[8 * u + 3], apply_relu));
-        q.z = pack_half2(relu_if(v[8 * u + 4], apply_relu), relu_if(v[8 * u + 5], apply_relu));
-        q.w = pack_half2(relu_if(v[8 * u + 6], apply_relu), relu_if(v[8 * u + 7], apply_relu));
+        q.x = pack2(relu_if(v[8 * u + 0], apply_relu), relu_if(v[8 * u + 1], apply_relu), bf16);
+        q.y = pack2(relu_if(v[8 * u + 2], apply_relu), relu_if(v[8 * u + 3], apply_relu), bf16);
+        q.z = pack2(relu_if(v[8 * u + 4], apply_relu), relu_if(v[8 * u + 5], apply_relu), bf16);
+        q.w = pack2(relu_if(v[8 * u + 6], apply_relu), relu_if(v[8 * u + 7], apply_relu), bf16);
         st_shared_v4(row_addr + ((u ^ (lane & 7u)) << 4), q);  // 128-byte swizzle
     }
     fence_proxy_async_smem();
@@ -358,12 +416,12 @@ __device__ __forceinline__ void sink_tma(const CUtensorMap* tmC, uint32_t stage_
 }
 
 // Swapped path: 16 accumulator columns (= C rows m0 .. m0+15) of C column n.
-__device__ __forceinline__ void sink_direct_swap(__half* C, const float* v, int32_t apply_relu,
-                                                 int64_t n, int64_t m0, int64_t M, int64_t N) {
+__device__ __forceinline__ void sink_direct_swap(uint16_t* C, const float* v, int32_t apply_relu,
+                                                 int32_t bf16, int64_t n, int64_t m0, int64_t M, int64_t N) {
     if (n >= N) return;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-        if (m0 + j < M) C[(m0 + j) * N + n] = __float2half_rn(relu_if(v[j], apply_relu));
+        if (m0 + j < M) C[(m0 + j) * N + n] = round16(relu_if(v[j], apply_relu), bf16);
 }
 
 template <int kMode>
@@ -385,7 +443,8 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     const gemm_relu_plan_t pl = p.plan;
     const int64_t M = p.M, N = p.N;
     const int32_t apply_relu = p.apply_relu;
-    __half* const C = p.C;
+    uint16_t* const C = p.C;
+    const int32_t out_bf16 = p.out_bf16;
     float* const ws = p.ws;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
@@ -413,12 +472,12 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     auto sink = [&](const WorkItem& it, uint32_t c) {
         if constexpr (T::kSwap) {
             if (swap_col < pl.tile_n)
-                sink_direct_swap(C, v, apply_relu, (int64_t)it.tn * pl.tile_n + swap_col,
+                sink_direct_swap(C, v, apply_relu, out_bf16, (int64_t)it.tn * pl.tile_n + swap_col,
                                  (int64_t)it.tm * pl.tile_m + c, M, N);
         } else {
             const int64_t row0 = (int64_t)it.tm * T::kTileM + 128 * half + 32 * quarter;
             const int64_t col = (int64_t)it.tn * T::kBN + c;
-            sink_tma(tmC, my_staging + sbuf * 4096u, lane, v, apply_relu, col, row0, M, N);
+            sink_tma(tmC, my_staging + sbuf * 4096u, lane, v, apply_relu, out_bf16, col, row0, M, N);
             sbuf ^= 1u;
         }
     };

@@ -175,12 +175,13 @@ int grow(void** buf, size_t* have, size_t need, cudaStream_t stream, bool zero) 
 }
 
 int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool bf16) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};  // bytes between rows
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims,
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -237,7 +238,7 @@ int check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N
 }
 
 int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-               int apply_relu, cudaStream_t st, int dev) {
+               int apply_relu, bool b_nk, bool bf16, cudaStream_t st, int dev) {
     DeviceState& d = g_dev[dev];
     if (M == 0 || N == 0) return GEMM_OK;
     if (K == 0) {
@@ -274,7 +275,9 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     kp.N = N;
     kp.K = K;
     kp.apply_relu = apply_relu ? 1 : 0;
-    kp.C = reinterpret_cast<__half*>(C);
+    kp.b_kmajor = b_nk ? 1 : 0;
+    kp.out_bf16 = bf16 ? 1 : 0;
+    kp.C = reinterpret_cast<uint16_t*>(C);
     kp.err = d.d_err;
     // generous bound: 2 s plus 2 us per k-block of the longest wait
     kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
@@ -293,24 +296,32 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     const bool swap = (pl.path == 3);
     // the swapped kernel's exchange buffer holds one peer's partial
     if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
-    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u);
+    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16);
     if (rc != GEMM_OK) return rc;
-    // B: 64-column boxes of one stage's block_k k-rows (a narrow swapped
-    // tile: one box of tile_n columns)
-    rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
-                   (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k);
+    if (!b_nk) {
+        // B (K, N): 64-column boxes of one stage's block_k k-rows (a narrow
+        // swapped tile: one box of tile_n columns)
+        rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
+                       (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k, bf16);
+    } else {
+        // B (N, K): boxes of 64 k by the rows of N one CTA loads per stage
+        const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
+                                   : (pl.path == 4 ? 128u : (uint32_t)pl.mma_n);
+        rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16);
+    }
     if (rc != GEMM_OK) return rc;
     // C: 64-column x 32-row boxes, one per epilogue warp and chunk
     CUtensorMap tc;
-    rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32);
+    rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32, bf16);
     if (rc != GEMM_OK) return rc;
     if (swap) {
-        // a narrow tile (<= 64 columns) runs M = 64 MMAs
-        kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/true,
-                                      /*b_mn=*/false);
+        // a narrow tile (<= 64 columns) runs M = 64 MMAs; B^T is MN-major
+        // when B is stored (K, N)
+        kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/!b_nk,
+                                      /*b_mn=*/false, bf16);
         return launch_mode<2>(d, pl, kp, ta, tb, tc, st);
     }
-    kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/true);
+    kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/!b_nk, bf16);
     if (pl.path == 4) return launch_mode<3>(d, pl, kp, ta, tb, tc, st);
     if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tc, st);
     return launch_mode<1>(d, pl, kp, ta, tb, tc, st);
@@ -321,8 +332,10 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
 
 using namespace gr;
 
-extern "C" int gemm_relu(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                         int apply_relu, void* stream) {
+extern "C" int gemm_relu_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                            int apply_relu, int b_layout, int dtype, void* stream) {
+    if ((b_layout != GEMM_B_KN && b_layout != GEMM_B_NK) || (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16))
+        return GEMM_ERR_INVALID_ARG;
     int rc = check_args(A, B, C, M, N, K, true);
     if (rc != GEMM_OK) return rc;
     if (M == 0 || N == 0) return GEMM_OK;  // nothing to enqueue
@@ -330,7 +343,13 @@ extern "C" int gemm_relu(const void* A, const void* B, void* C, int64_t M, int64
     if ((rc = current_device(&dev)) != GEMM_OK) return rc;
     std::lock_guard<std::mutex> lock(g_mu);
     if ((rc = init_device_locked(dev)) != GEMM_OK) return rc;
-    return run_device(A, B, C, M, N, K, apply_relu, reinterpret_cast<cudaStream_t>(stream), dev);
+    return run_device(A, B, C, M, N, K, apply_relu, b_layout == GEMM_B_NK, dtype == GEMM_DTYPE_BF16,
+                      reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+extern "C" int gemm_relu(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                         int apply_relu, void* stream) {
+    return gemm_relu_ex(A, B, C, M, N, K, apply_relu, GEMM_B_KN, GEMM_DTYPE_F16, stream);
 }
 
 extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
@@ -355,7 +374,7 @@ extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_ho
         if (rc == GEMM_OK && b_bytes &&
             cudaMemcpyAsync(sb.hB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
             rc = GEMM_ERR_CUDA;
-        if (rc == GEMM_OK) rc = run_device(sb.hA, sb.hB, sb.hC, M, N, K, apply_relu, st, dev);
+        if (rc == GEMM_OK) rc = run_device(sb.hA, sb.hB, sb.hC, M, N, K, apply_relu, false, false, st, dev);
         if (rc == GEMM_OK &&
             cudaMemcpyAsync(C_host, sb.hC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
             rc = GEMM_ERR_CUDA;

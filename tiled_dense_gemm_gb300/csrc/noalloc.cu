@@ -160,7 +160,7 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     kp.N = N;
     kp.K = K;
     kp.apply_relu = apply_relu ? 1 : 0;
-    kp.C = reinterpret_cast<__half*>(C);
+    kp.C = reinterpret_cast<uint16_t*>(C);
     kp.err = reinterpret_cast<int32_t*>(s.scratch);
     kp.counters = reinterpret_cast<uint32_t*>(s.scratch + kCounterOffset);
     kp.ws = reinterpret_cast<float*>(s.scratch + kPartialOffset);

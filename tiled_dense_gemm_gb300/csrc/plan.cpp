@@ -414,7 +414,7 @@ extern "C" int gemm_relu_plan_work_item(const gemm_relu_plan_t* plan, int cta, i
         wi.init(*plan, cta / plan->cluster, cta % plan->cluster);
     else
         wi.init(*plan, cta);
-    WorkItem w;
+    WorkItem w = {};
     for (int i = 0; i <= idx; ++i)
         if (!wi.next(*plan, w)) return 0;
     if (tile) *tile = w.tile;

@@ -397,13 +397,16 @@ __host__ __device__ __forceinline__ uint64_t make_sw128_desc(uint32_t smem_addr,
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma kind::f16 with fp16 A/B and fp32 D:
-//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16), 10-12 B format,
-//   bit 15 A is MN-major, bit 16 B is MN-major, 17-22 N >> 3, 24-28 M >> 4.
+// Instruction descriptor for tcgen05.mma kind::f16 with fp32 D:
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always the same type), bit 15 A is MN-major, bit 16 B
+//   is MN-major, 17-22 N >> 3, 24-28 M >> 4.
 __host__ __device__ __forceinline__ uint32_t make_idesc_f16_f32(uint32_t m, uint32_t n,
-                                                                bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-           ((n >> 3) << 17) | ((m >> 4) << 24);
+                                                                bool a_mn_major, bool b_mn_major,
+                                                                bool bf16 = false) {
+    const uint32_t fmt = bf16 ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 }  // namespace gr

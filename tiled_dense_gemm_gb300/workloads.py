@@ -1,6 +1,6 @@
 """Seeded synthetic inputs for C = ReLU(A . B).
 
-This module only draws random binary16 matrices; it holds none of the
+This module only draws random binary16 (or bfloat16) matrices; it holds none of the
 product's arithmetic, so both the CUDA path and the CPU oracle can consume
 the same bytes without sharing any compute code.
 
@@ -67,26 +67,33 @@ WORKLOADS = {
 }
 
 
-def _draw(g: torch.Generator, shape, dist: str, scale: float) -> torch.Tensor:
+def _draw(g: torch.Generator, shape, dist: str, scale: float, dtype=torch.float16) -> torch.Tensor:
     if dist == "normal":
         x = torch.randn(shape, generator=g, dtype=torch.float32)
     elif dist == "uniform":
         x = torch.rand(shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
     elif dist == "intgrid":
         r = int(scale)
-        return torch.randint(-r, r + 1, shape, generator=g, dtype=torch.int32).to(torch.float16)
+        return torch.randint(-r, r + 1, shape, generator=g, dtype=torch.int32).to(dtype)
     else:
         raise ValueError(f"unknown distribution {dist!r}")
-    return (x * scale).to(torch.float16)
+    return (x * scale).to(dtype)
 
 
 def make_inputs(M: int, N: int, K: int, seed: int, dist_a: str = "normal",
-                scale_a: float = 1.0, dist_b: str = "normal", scale_b: float = 1.0):
-    """Return (A, B): CPU binary16 tensors of shapes (M, K) and (K, N)."""
+                scale_a: float = 1.0, dist_b: str = "normal", scale_b: float = 1.0,
+                dtype=torch.float16, b_layout: str = "kn"):
+    """Return (A, B): CPU tensors of shapes (M, K) and (K, N), rounded once to
+    ``dtype`` (binary16 or bfloat16).  With ``b_layout="nk"`` B is returned
+    stored as its (N, K) transpose, same values (drawn in the (K, N) order)."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
-    a = _draw(g, (M, K), dist_a, scale_a).contiguous()
-    b = _draw(g, (K, N), dist_b, scale_b).contiguous()
+    a = _draw(g, (M, K), dist_a, scale_a, dtype).contiguous()
+    b = _draw(g, (K, N), dist_b, scale_b, dtype).contiguous()
+    if b_layout == "nk":
+        b = b.t().contiguous()
+    elif b_layout != "kn":
+        raise ValueError(f"unknown B layout {b_layout!r}")
     return a, b
 
 
