@@ -167,7 +167,7 @@ int gemm_relu_noalloc(const void* A, const void* B, void* C,
 
 typedef struct {
     int32_t path;        /* 0 nothing to do, 1 zero fill (K == 0), 2 tiled (one CTA per tile),
-                            3 swapped operands (small M), 4 tiled by CTA pairs (256 x 256) */
+                            3 swapped operands (small M), 4 tiled by CTA pairs (256 x mma_n) */
     int32_t mma_m;       /* tcgen05 MMA M: 128, or 256 for a CTA pair (C rows; C columns for path 3) */
     int32_t mma_n;       /* tcgen05 MMA N: 128 or 256 (C columns) / padded M (path 3) */
     int32_t tile_m;      /* C tile rows */
@@ -200,8 +200,9 @@ typedef struct {
  * num_sms / 2; the runtime also caps them by the device's co-resident
  * cluster count).  Pure host code.  The environment variable
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
- * "tiled256", "tiled128", "swap" (M <= 128 only), "swapnW" (M <= 128,
- * data-parallel tiles W = 8..64 columns wide) or "pair", optionally
+ * "tiled256", "tiled128", "tiled64" (128 x 64 tiles), "swap" (M <= 128 only), "swapnW" (M <= 128,
+ * data-parallel tiles W = 8..64 columns wide), "pair" (CTA pairs, 256 x
+ * 256 tiles) or "pair128" (CTA pairs, 256 x 128 tiles), optionally
  * followed by ":dp" to forbid splitting tiles along K, by ":sN" to cut
  * every tile into N equal K ranges (the split schedule), or by ":c2" to
  * split every tile's K range between the two CTAs of a cluster, which

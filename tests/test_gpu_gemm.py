@@ -264,7 +264,8 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "tiled128:dp",
                                    "pair:dp", "swap", "swap:dp", "swap:s7", "swapn56", "swapn8",
                                    "tiled128:s3", "pair:s5", "tiled128:c2", "tiled256:c2", "swap:c2",
-                                   "swap:sk", "tiled128:sk"])
+                                   "swap:sk", "tiled128:sk", "pair128", "pair128:dp", "pair128:s3",
+                                   "tiled64", "tiled64:s3", "tiled64:c2"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands with 128-wide or narrow tiles), with and without

@@ -86,15 +86,17 @@ struct KParams {
 // kMode 0: C tile 128 x 256; 1: C tile 128 x 128; 2: swapped operands
 // (C tile mpad x 128: B^T is the MMA A operand, A^T the MMA B operand);
 // 3: CTA pair, C tile 256 x 256 (each CTA holds 128 rows of A, 128 columns
-// of B, and accumulates its 128 rows x 256 columns).
+// of B, and accumulates its 128 rows x 256 columns); 4: CTA pair, C tile
+// 256 x 128 (each CTA holds 128 rows of A and 64 columns of B); 5: C tile
+// 128 x 64.
 template <int kMode>
 struct ModeTraits {
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr bool kPair = (kMode == 3);
+    static constexpr bool kPair = (kMode == 3 || kMode == 4);
     static constexpr int kCG = kPair ? 2 : 1;
-    static constexpr uint32_t kBN = (kMode == 1) ? 128 : 256;  // C columns per tile (normal)
+    static constexpr uint32_t kBN = (kMode == 5) ? 64 : (kMode == 1 || kMode == 4) ? 128 : 256;  // C columns per tile
     static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
-    static constexpr uint32_t kBCols = kPair ? 128 : kBN;      // B columns loaded per CTA
+    static constexpr uint32_t kBCols = kPair ? kBN / 2 : kBN;  // B columns loaded per CTA
     // k-rows per ring stage (the plan's block_k): the swapped kernel's
     // small MMAs take 128 per stage, the others 64
     static constexpr uint32_t kBK = kSwap ? 2 * kBlockK : kBlockK;
@@ -214,7 +216,7 @@ struct Producer {
                 // first row of A and first column of B this CTA loads
                 if constexpr (T::kPair) {
                     a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
-                    b_col = w.tn * (int32_t)T::kBN + 128 * (int32_t)rank;
+                    b_col = w.tn * (int32_t)T::kBN + (int32_t)T::kBCols * (int32_t)rank;
                 } else if constexpr (!T::kSwap) {
                     a_row = w.tm * 128;
                     b_col = w.tn * (int32_t)T::kBN;
@@ -233,7 +235,7 @@ struct Producer {
                 if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
                 tma_load_2d_pair(a_dst, tmA, full_leader, k0, a_row);
                 if (b_nk) {
-                    tma_load_2d_pair(b_dst, tmB, full_leader, k0, b_col);  // this CTA's 128 rows of B
+                    tma_load_2d_pair(b_dst, tmB, full_leader, k0, b_col);  // this CTA's kBCols rows of B
                 } else {
 #pragma unroll
                     for (uint32_t j = 0; j < T::kBCols / 64; ++j)

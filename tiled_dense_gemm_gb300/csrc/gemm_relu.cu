@@ -46,7 +46,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[4] = {false, false, false, false};
+    bool attr_set[6] = {false, false, false, false, false, false};
     std::vector<StreamBuffers> streams;
 };
 
@@ -306,7 +306,7 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     } else {
         // B (N, K): boxes of 64 k by the rows of N one CTA loads per stage
         const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
-                                   : (pl.path == 4 ? 128u : (uint32_t)pl.mma_n);
+                                   : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
         rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16);
     }
     if (rc != GEMM_OK) return rc;
@@ -322,8 +322,10 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         return launch_mode<2>(d, pl, kp, ta, tb, tc, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/!b_nk, bf16);
-    if (pl.path == 4) return launch_mode<3>(d, pl, kp, ta, tb, tc, st);
+    if (pl.path == 4) return pl.mma_n == 128 ? launch_mode<4>(d, pl, kp, ta, tb, tc, st)
+                                             : launch_mode<3>(d, pl, kp, ta, tb, tc, st);
     if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tc, st);
+    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, ta, tb, tc, st);
     return launch_mode<1>(d, pl, kp, ta, tb, tc, st);
 }
 

@@ -42,16 +42,26 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     // measured: ~1 us of handshake + the peer's 128 x mma_n fp32 tile at
     // ~32 B/clk over DSMEM, plus the cluster teardown
     c.exchange = 1.0 + 128.0 * mma_n * 4.0 / 32000.0;
-    if (path == 4) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
+    if (path == 4 && mma_n >= 256) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
         c.kb = 0.29;
         c.tile_store = 2.5;
         c.partial = 6.0;
         c.reduce_per_slot = 4.0;
+    } else if (path == 4) {  // CTA pair, 256 x 128 (each CTA 128 x 128): measured no faster
+        c.kb = 0.31;         // per k-block than one CTA per 128 x 128 tile
+        c.tile_store = 1.3;
+        c.partial = 3.0;
+        c.reduce_per_slot = 2.0;
     } else if (path == 2 && mma_n >= 256) {
         c.kb = 0.37;
         c.tile_store = 2.5;
         c.partial = 6.0;
         c.reduce_per_slot = 4.0;
+    } else if (path == 2 && mma_n <= 64) {  // 128 x 64
+        c.kb = 0.20;
+        c.tile_store = 0.7;
+        c.partial = 1.5;
+        c.reduce_per_slot = 1.0;
     } else if (path == 2) {
         c.kb = 0.30;
         c.tile_store = 1.3;
@@ -296,17 +306,25 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // for 32 < M <= 64 only where it splits K without stream-K (below);
     // else, and above, the 128 x 128 tiled kernel measured faster
     bool want_swap = M <= 64, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
+    bool want_pair128 = want_pair, want_t64 = want_t128;
     const bool swap_only = M <= 32 || starts_with(f, "swap");
     if (starts_with(f, "swap") && M <= 128) {
-        want_t256 = want_t128 = want_pair = false;
+        want_t256 = want_t128 = want_pair = want_pair128 = want_t64 = false;
         want_swap = true;
     } else if (starts_with(f, "tiled256")) {
-        want_swap = want_t128 = want_pair = false;
+        want_swap = want_t128 = want_pair = want_pair128 = want_t64 = false;
         want_t256 = true;
+    } else if (starts_with(f, "tiled64")) {
+        want_swap = want_t256 = want_t128 = want_pair = want_pair128 = false;
+        want_t64 = true;
     } else if (starts_with(f, "tiled128")) {
-        want_swap = want_t256 = want_pair = false;
+        want_swap = want_t256 = want_pair = want_pair128 = want_t64 = false;
         want_t128 = true;
+    } else if (starts_with(f, "pair128") && pairs > 0) {
+        want_swap = want_t256 = want_t128 = want_pair = want_t64 = false;
+        want_pair128 = true;
     } else if (starts_with(f, "pair") && pairs > 0) {
+        want_pair128 = want_t64 = false;
         want_swap = want_t256 = want_t128 = false;
         want_pair = true;
     }
@@ -386,8 +404,10 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         if (swap_only) take(3, mpad, num_sms);
     }
     if (want_pair) take(4, 256, pairs);
+    if (want_pair128) take(4, 128, pairs);
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
+    if (want_t64) take(2, 64, num_sms);
     return GEMM_OK;
 }
 
