@@ -5,9 +5,13 @@ One step = one gemm_relu call over one input set of the workload (default:
 M = N = K = 1024, A, B ~ N(0, 1), seed 1 -- the worked size of the
 GEMM+ReLU tutorial listing).  Inputs rotate over enough seeded sets that
 their total exceeds twice the 129 MB L2, so no step starts with its inputs
-in L2.  Device timing uses CUDA events on the launching stream; launches are
-queued behind a short device-side sleep so that per-launch events measure
-the kernel and not Python.
+in L2.  Device timing uses CUDA events on the launching stream: K launches
+back to back between one event pair (queued behind a short device-side
+sleep, so the events measure the device and not Python); a second pass
+with an event pair around each launch gives the per-launch min / median
+reported beside it.  The other workloads, a labelled hot-L2 figure for the
+skinny shape, and the CPU oracle's rate on every workload (all cores; one
+core for the two small ones) are reported in the same line.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
 the host cores instead (the slow reference arm).
@@ -211,8 +215,50 @@ def time_device(w, device, steps, warmup, world):
     barrier(world)
     binding.check_device_error(stream)
     total = start.elapsed_time(end)
+    # Second pass, reported beside the back-to-back figure: an event pair
+    # around each launch (>= 100 launches), for the per-launch min / median.
+    n_each = max(steps, 100)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_each)]
+    torch.cuda.synchronize(device)
+    torch.cuda._sleep(int(max(4_000_000, n_each * 1_000_000)))
+    for i, (e0, e1) in enumerate(evs):
+        a, b, c = sets[i % len(sets)]
+        e0.record(stream)
+        binding.gemm_relu(a, b, c, relu, stream)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    binding.check_device_error(stream)
+    each = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
     return {"total_ms": total, "launch_ms": total / steps, "sets": len(sets),
-            "set_bytes": 2 * (w.M * w.K + w.K * w.N)}
+            "set_bytes": 2 * (w.M * w.K + w.K * w.N),
+            "per_launch_event_us": {"launches": n_each, "min": each[0] * 1e3,
+                                    "median": each[len(each) // 2] * 1e3}}
+
+
+def time_hot_l2(w, device, steps):
+    """The same input set every launch (operands may stay in L2): a labelled
+    hot-L2 figure, not the headline."""
+    import torch
+    from tiled_dense_gemm_gb300 import binding
+    from tiled_dense_gemm_gb300.workloads import workload_inputs
+    A, B = workload_inputs(w)
+    a, b = A.to(device), B.to(device)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        binding.gemm_relu(a, b, c, True, stream)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    torch.cuda._sleep(int(max(4_000_000, steps * 1_000_000)))
+    start.record(stream)
+    for _ in range(steps):
+        binding.gemm_relu(a, b, c, True, stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    binding.check_device_error(stream)
+    return start.elapsed_time(end) / steps
 
 
 def soak(w, device, seconds):
@@ -380,7 +426,7 @@ def run_ours(args, w):
 
     others = {}
     if not args.no_extra and rank == 0:
-        for name in ("c3_4096", "c4_skinny"):
+        for name in ("c1_256", "c2_1024", "c3_4096", "c4_skinny", "c5_ragged"):
             if name == w.name:
                 continue
             wo = WORKLOADS[name]
@@ -390,19 +436,42 @@ def run_ours(args, w):
             ro = roofline_for(wo, ms, p2)
             others[name] = {"workload": workload_summary(wo), "tflops": wo.flops / (ms * 1e-3) / 1e12,
                             "avg_launch_us": ms * 1e3, "roofline": ro,
+                            "per_launch_event_us": r2["per_launch_event_us"],
+                            "plan": {k: p2[k] for k in ("path", "mma_n", "grid", "cluster", "splits",
+                                                        "sk_tiles")},
                             "steps": max(args.steps, 20)}
+            if name == "c4_skinny":
+                hot = time_hot_l2(wo, device, max(args.steps, 20))
+                others[name]["hot_l2"] = {
+                    "avg_launch_us": hot * 1e3,
+                    "gbs": wo.algorithmic_bytes / (hot * 1e-3) / 1e9,
+                    "note": "one input set reused every launch: B may be partly L2-resident; "
+                            "not the headline"}
             torch.cuda.empty_cache()
 
     e2e_ms = time_e2e(w, args.steps, args.warmup, device)
     e2e_ms = reduce_max_over_ranks(e2e_ms, world, device)
 
     cpu = None
+    cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         oracle.build()
         threads = len(os.sched_getaffinity(0))
         rate, desc, _ = cpu_oracle_rate(w, args.cpu_seconds, threads)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+        if not args.no_extra:
+            # every workload on all cores, and c1 / c2 on one core (bounded
+            # samples of ~2 s each; compiled with -O2, no fast-math)
+            cpu_all = {"flags": "gcc -O2 -fno-fast-math -ffp-contract=off -fopenmp"}
+            for name in ("c1_256", "c2_1024", "c3_4096", "c4_skinny", "c5_ragged"):
+                wo = WORKLOADS[name]
+                r_all, d_all, _ = cpu_oracle_rate(wo, 2.0, threads)
+                entry = {"all_cores": {"tflops": r_all, "cores": threads, "sample": d_all}}
+                if name in ("c1_256", "c2_1024"):
+                    r_one, d_one, _ = cpu_oracle_rate(wo, 2.0, 1)
+                    entry["one_core"] = {"tflops": r_one, "cores": 1, "sample": d_one}
+                cpu_all[name] = entry
 
     if rank == 0:
         line = {
@@ -426,6 +495,8 @@ def run_ours(args, w):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "cpu_oracle_by_workload": cpu_all,
+            "per_launch_event_us": res["per_launch_event_us"],
             "other_workloads": others,
         }
         print(json.dumps(line), flush=True)
