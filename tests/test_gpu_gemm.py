@@ -107,6 +107,20 @@ def test_ragged_sampled_parity(relu):
     assert_relu_sign(C, relu)
 
 
+@pytest.mark.parametrize("force", ["pair:t2", "pair:t3", "pair:t4", "tiled256:t2", "tiled128:t3"])
+def test_split_tail_wave_sampled(monkeypatch, force):
+    """Full waves data-parallel and the leftover tiles split along K (the
+    tail wave), on the ragged workload: sampled rows and columns, ReLU on
+    and off, and the split-K counters left at zero for the next call."""
+    w = WORKLOADS["c5_ragged"]
+    A, B = workload_inputs(w)
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    for relu in (True, False):
+        C = gpu_run(A, B, relu)
+        check_sampled(A, B, C, relu, 6, f"c5_ragged {force} relu={relu}")
+        assert_relu_sign(C, relu)
+
+
 def test_ragged_tail_block_full():
     """The whole last tile row and tile column of the ragged workload."""
     w = WORKLOADS["c5_ragged"]

@@ -150,6 +150,18 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert d["splits"] == (want_s if want_s > 1 else 1)
 
 
+@pytest.mark.parametrize("force,sp", [("pair:t2", 2), ("pair:t3", 3), ("tiled256:t4", 4)])
+def test_tail_wave_split(gemm_lib, monkeypatch, force, sp):
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    for shape in [(4096, 4096, 4096), (3000, 5000, 2056), (8192, 8192, 2048)]:
+        d = _check(gemm_lib, *shape, 152, forced=True)
+        workers = d["grid"]
+        T = d["num_tiles"]
+        if T % workers:
+            assert d["dp_tiles"] == (T // workers) * workers
+            assert d["sk_tiles"] == T % workers and d["splits"] == sp and d["max_slots"] == sp
+
+
 def test_random_shapes(gemm_lib):
     rng = random.Random(0)
     for _ in range(60):

@@ -243,6 +243,18 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, i
         if (T >= workers) {
             const int32_t full = T / workers;
             if (T % workers != 0) consider(workers, (full - 1) * workers, T - (full - 1) * workers);
+            // full waves data-parallel, the leftover tiles cut into S equal
+            // K ranges spread over the workers (a short split-K tail wave)
+            if (T % workers != 0)
+                for (int32_t sp = 2; sp <= 4 && sp <= p.num_kb; ++sp) {
+                    gemm_relu_plan_t q = p;
+                    finish_split(q, workers, full * workers, T % workers, sp);
+                    const double cost = estimate(q, c) + 1e-3 * (double)q.sk_tiles;
+                    if (best_cost < 0.0 || cost < best_cost) {
+                        best_cost = cost;
+                        best = q;
+                    }
+                }
         } else if (p.num_kb > 1 && operands_fit_l2) {
             // fewer tiles than workers: split every tile along K over more
             // workers.  Only when A and B stay in L2: the workers sharing a
@@ -290,6 +302,9 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     const bool dp_only = contains(f, ":dp");
     const bool force_csk = contains(f, ":c2");
     const bool force_sk = contains(f, ":sk");
+    int32_t force_tail = 0;  // ":tS": full waves data-parallel, leftover tiles split S ways
+    for (const char* q = f; *q; ++q)
+        if (q[0] == ':' && q[1] == 't' && q[2] >= '0' && q[2] <= '9') force_tail = q[2] - '0';
     int32_t force_splits = 0;
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 's' && q[2] >= '0' && q[2] <= '9') {
@@ -335,6 +350,12 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         memset(&q, 0, sizeof(q));
         shape_plan(q, M, N, K, path, mma_n);
         double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2, pairs);
+        if (force_tail > 1 && q.num_tiles >= workers && q.num_tiles % workers != 0) {
+            q.cluster = (path == 4) ? 2 : 1;
+            const int32_t sp = force_tail < q.num_kb ? force_tail : q.num_kb;
+            finish_split(q, workers, (q.num_tiles / workers) * workers, q.num_tiles % workers, sp);
+            cost = 0.0;
+        }
         if (force_sk) {
             // every tile stream-K over all workers
             const int64_t units = (int64_t)q.num_tiles * q.num_kb;
