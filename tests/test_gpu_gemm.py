@@ -107,7 +107,8 @@ def test_ragged_sampled_parity(relu):
     assert_relu_sign(C, relu)
 
 
-@pytest.mark.parametrize("force", ["pair:t2", "pair:t3", "pair:t4", "tiled256:t2", "tiled128:t3"])
+@pytest.mark.parametrize("force", ["pair:t2", "pair:t3", "pair:t4", "tiled256:t2", "tiled128:t3", "pair192",
+                                   "pair192:t2"])
 def test_split_tail_wave_sampled(monkeypatch, force):
     """Full waves data-parallel and the leftover tiles split along K (the
     tail wave), on the ragged workload: sampled rows and columns, ReLU on
@@ -279,7 +280,7 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
                                    "pair:dp", "swap", "swap:dp", "swap:s7", "swapn56", "swapn8",
                                    "tiled128:s3", "pair:s5", "tiled128:c2", "tiled256:c2", "swap:c2",
                                    "swap:sk", "tiled128:sk", "pair128", "pair128:dp", "pair128:s3",
-                                   "tiled64", "tiled64:s3", "tiled64:c2"])
+                                   "tiled64", "tiled64:s3", "tiled64:c2", "pair192", "pair192:s3"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands with 128-wide or narrow tiles), with and without

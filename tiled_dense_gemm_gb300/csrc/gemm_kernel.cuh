@@ -88,15 +88,24 @@ struct KParams {
 // 3: CTA pair, C tile 256 x 256 (each CTA holds 128 rows of A, 128 columns
 // of B, and accumulates its 128 rows x 256 columns); 4: CTA pair, C tile
 // 256 x 128 (each CTA holds 128 rows of A and 64 columns of B); 5: C tile
-// 128 x 64.
+// 128 x 64; 6: CTA pair, C tile 256 x 192 (each CTA holds 96 columns of B:
+// one 64-wide chunk and a half-filled one, whose 32 columns come through a
+// second tensor map of B when B is stored (K, N)).
 template <int kMode>
 struct ModeTraits {
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr bool kPair = (kMode == 3 || kMode == 4);
+    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6);
     static constexpr int kCG = kPair ? 2 : 1;
-    static constexpr uint32_t kBN = (kMode == 5) ? 64 : (kMode == 1 || kMode == 4) ? 128 : 256;  // C columns per tile
+    static constexpr uint32_t kBN = (kMode == 5)                   ? 64
+                                    : (kMode == 1 || kMode == 4) ? 128
+                                    : (kMode == 6)               ? 192
+                                                                 : 256;  // C columns per tile
     static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
     static constexpr uint32_t kBCols = kPair ? kBN / 2 : kBN;  // B columns loaded per CTA
+    // (K, N) storage: full 64-wide chunks of B per CTA, and the width of a
+    // last partial one (0 if none)
+    static constexpr uint32_t kBFull = kBCols / 64, kBRem = kBCols % 64;
+    static constexpr uint32_t kBChunks = kBFull + (kBRem ? 1 : 0);
     // k-rows per ring stage (the plan's block_k): the swapped kernel's
     // small MMAs take 128 per stage, the others 64
     static constexpr uint32_t kBK = kSwap ? 2 * kBlockK : kBlockK;
@@ -170,6 +179,7 @@ struct Producer {
     Ctrl* ctrl;
     const CUtensorMap* tmA;
     const CUtensorMap* tmB;
+    const CUtensorMap* tmB2;  // (K, N) storage: boxes of the last partial chunk (pair, 256 x 192)
     gemm_relu_plan_t pl;
     uint32_t stages, stride, a_bytes, rank, S, full0, empty0, tx_bytes;
     WorkIter wi;
@@ -187,8 +197,8 @@ struct Producer {
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
-                                        int32_t worker, uint32_t rank_)
-        : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), pl(p_.plan), stages(stages_), stride(stride_),
+                                        const CUtensorMap* tmB2_, int32_t worker, uint32_t rank_)
+        : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), tmB2(tmB2_), pl(p_.plan), stages(stages_), stride(stride_),
           a_bytes(a_bytes_), rank(rank_), have_item(false), kb(0), a_row(0), b_col(0), s(0), ph(0) {
         S = (uint32_t)pl.num_stages;
         full0 = smem_u32(&ctrl->full[0]);
@@ -238,8 +248,11 @@ struct Producer {
                     tma_load_2d_pair(b_dst, tmB, full_leader, k0, b_col);  // this CTA's kBCols rows of B
                 } else {
 #pragma unroll
-                    for (uint32_t j = 0; j < T::kBCols / 64; ++j)
+                    for (uint32_t j = 0; j < T::kBFull; ++j)
                         tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                    if constexpr (T::kBRem != 0)
+                        tma_load_2d_pair(b_dst + T::kBFull * kChunkBytes, tmB2, full_leader,
+                                         b_col + 64 * (int32_t)T::kBFull, k0);
                 }
             } else {
                 mbar_arrive_expect_tx(full, tx_bytes);
@@ -724,7 +737,8 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ KParams p) {
     using T = ModeTraits<kMode>;
     extern __shared__ __align__(1024) uint8_t smem[];
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem);
@@ -735,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of B columns (kBK k-rows) per 64 tile columns (a narrow tile, at most
     // 64 columns, takes one chunk and an M = 64 MMA)
     const uint32_t a_bytes = T::kSwap ? (pl.tile_n <= 64 ? 1u : 2u) * T::kBK * kSwizzleRow : kOperandA;
-    const uint32_t b_bytes = (T::kPair ? T::kBCols * kBlockK * 2
+    const uint32_t b_bytes = (T::kPair ? T::kBChunks * kChunkBytes
                                        : ((uint32_t)pl.mma_n * T::kBK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -747,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (T::kBRem != 0) tma_prefetch_desc(&tmB2);
         if constexpr (!T::kSwap) tma_prefetch_desc(&tmC);
         for (int s = 0; s < pl.num_stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
@@ -783,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, worker, rank);
+            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
             prod.issue(-1);
         }
         __syncwarp();

@@ -46,7 +46,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[6] = {false, false, false, false, false, false};
+    bool attr_set[7] = {false, false, false, false, false, false, false};
     std::vector<StreamBuffers> streams;
 };
 
@@ -190,7 +190,7 @@ int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
 
 template <int kMode>
 int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, const CUtensorMap& ta,
-                const CUtensorMap& tb, const CUtensorMap& tc, cudaStream_t st) {
+                const CUtensorMap& tb, const CUtensorMap& tb2, const CUtensorMap& tc, cudaStream_t st) {
     auto fn = gemm_relu_kernel<kMode>;
     if (!d.attr_set[kMode]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) !=
@@ -214,7 +214,7 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, kp) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tb2, tc, kp) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -298,16 +298,25 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
     int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16);
     if (rc != GEMM_OK) return rc;
+    CUtensorMap tb2;
     if (!b_nk) {
         // B (K, N): 64-column boxes of one stage's block_k k-rows (a narrow
         // swapped tile: one box of tile_n columns)
         rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
                        (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k, bf16);
+        // a pair CTA whose B columns end in a partial chunk (256 x 192
+        // tiles: 96 columns) loads that chunk with narrower boxes
+        const uint32_t rem = (pl.path == 4) ? (uint32_t)(pl.mma_n / 2) % 64u : 0u;
+        if (rc == GEMM_OK && rem)
+            rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, rem, (uint32_t)pl.block_k, bf16);
+        else
+            tb2 = tb;
     } else {
         // B (N, K): boxes of 64 k by the rows of N one CTA loads per stage
         const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
                                    : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
         rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16);
+        tb2 = tb;
     }
     if (rc != GEMM_OK) return rc;
     // C: 64-column x 32-row boxes, one per epilogue warp and chunk
@@ -319,14 +328,17 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         // when B is stored (K, N)
         kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/!b_nk,
                                       /*b_mn=*/false, bf16);
-        return launch_mode<2>(d, pl, kp, ta, tb, tc, st);
+        return launch_mode<2>(d, pl, kp, ta, tb, tb2, tc, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/!b_nk, bf16);
-    if (pl.path == 4) return pl.mma_n == 128 ? launch_mode<4>(d, pl, kp, ta, tb, tc, st)
-                                             : launch_mode<3>(d, pl, kp, ta, tb, tc, st);
-    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tc, st);
-    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, ta, tb, tc, st);
-    return launch_mode<1>(d, pl, kp, ta, tb, tc, st);
+    if (pl.path == 4) {
+        if (pl.mma_n == 128) return launch_mode<4>(d, pl, kp, ta, tb, tb2, tc, st);
+        if (pl.mma_n == 192) return launch_mode<6>(d, pl, kp, ta, tb, tb2, tc, st);
+        return launch_mode<3>(d, pl, kp, ta, tb, tb2, tc, st);
+    }
+    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tb2, tc, st);
+    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, ta, tb, tb2, tc, st);
+    return launch_mode<1>(d, pl, kp, ta, tb, tb2, tc, st);
 }
 
 }  // namespace

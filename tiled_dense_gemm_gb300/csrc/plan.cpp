@@ -47,6 +47,11 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
         c.tile_store = 2.5;
         c.partial = 6.0;
         c.reduce_per_slot = 4.0;
+    } else if (path == 4 && mma_n == 192) {  // CTA pair, 256 x 192: measured no faster per
+        c.kb = 0.32;                          // k-block than 256 x 256 (the MMA warp's loop bounds both)
+        c.tile_store = 1.9;
+        c.partial = 4.5;
+        c.reduce_per_slot = 3.0;
     } else if (path == 4) {  // CTA pair, 256 x 128 (each CTA 128 x 128): measured no faster
         c.kb = 0.31;         // per k-block than one CTA per 128 x 128 tile
         c.tile_store = 1.3;
@@ -177,7 +182,11 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     // bytes the TMA copies of one stage deliver
     const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * p.block_k * 2 : kOperandABytes;
     p.stage_bytes = a_box_bytes + b_bytes;
-    const int32_t stride = a_region + ((b_bytes + 1023) / 1024) * 1024;
+    // B region: a pair CTA's (K, N) chunks are 64 columns wide, the last
+    // one possibly partial (256 x 192 tiles: 96 columns = 1.5 chunks)
+    const int32_t b_region = (path == 4) ? ((b_cols + 63) / 64) * 64 * p.block_k * 2
+                                         : ((b_bytes + 1023) / 1024) * 1024;
+    const int32_t stride = a_region + b_region;
     // tiled paths: C staging for the TMA stores; swapped: the buffer a
     // cluster split-K peer pushes its fp32 partial into (128 x mma_n)
     const int32_t staging = (path == 3) ? 128 * mma_n * 4 : kStagingBytes;
@@ -321,25 +330,28 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // for 32 < M <= 64 only where it splits K without stream-K (below);
     // else, and above, the 128 x 128 tiled kernel measured faster
     bool want_swap = M <= 64, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
-    bool want_pair128 = want_pair, want_t64 = want_t128;
+    bool want_pair128 = want_pair, want_t64 = want_t128, want_pair192 = want_pair;
     const bool swap_only = M <= 32 || starts_with(f, "swap");
     if (starts_with(f, "swap") && M <= 128) {
-        want_t256 = want_t128 = want_pair = want_pair128 = want_t64 = false;
+        want_t256 = want_t128 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
         want_swap = true;
     } else if (starts_with(f, "tiled256")) {
-        want_swap = want_t128 = want_pair = want_pair128 = want_t64 = false;
+        want_swap = want_t128 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
         want_t256 = true;
     } else if (starts_with(f, "tiled64")) {
-        want_swap = want_t256 = want_t128 = want_pair = want_pair128 = false;
+        want_swap = want_t256 = want_t128 = want_pair = want_pair128 = want_pair192 = false;
         want_t64 = true;
     } else if (starts_with(f, "tiled128")) {
-        want_swap = want_t256 = want_pair = want_pair128 = want_t64 = false;
+        want_swap = want_t256 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
         want_t128 = true;
+    } else if (starts_with(f, "pair192") && pairs > 0) {
+        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair128 = false;
+        want_pair192 = true;
     } else if (starts_with(f, "pair128") && pairs > 0) {
-        want_swap = want_t256 = want_t128 = want_pair = want_t64 = false;
+        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair192 = false;
         want_pair128 = true;
     } else if (starts_with(f, "pair") && pairs > 0) {
-        want_pair128 = want_t64 = false;
+        want_pair128 = want_t64 = want_pair192 = false;
         want_swap = want_t256 = want_t128 = false;
         want_pair = true;
     }
@@ -426,6 +438,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     }
     if (want_pair) take(4, 256, pairs);
     if (want_pair128) take(4, 128, pairs);
+    if (want_pair192) take(4, 192, pairs);
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
     if (want_t64) take(2, 64, num_sms);
