@@ -50,10 +50,10 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     else:
         assert d["mma_n"] in (128, 192, 256)
         assert (d["mma_m"], d["tile_m"], d["tile_n"], d["cluster"]) == (256, 256, d["mma_n"], 2)
-        assert d["stage_bytes"] == 16384 + d["mma_n"] // 2 * 128
+        assert d["stage_bytes"] == (128 + d["mma_n"] // 2) * d["block_k"] * 2
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
     assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
-    assert d["block_k"] == (128 if d["path"] == 3 else 64)
+    assert d["block_k"] == (64 if (d["path"] in (2, 4) and d["mma_n"] == 256) else 128)
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
     assert d["smem_bytes"] <= SMEM_LIMIT

@@ -43,10 +43,9 @@ constexpr int kThreads = 192;
 constexpr uint32_t kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;  // named barrier id for the epilogue warps
 constexpr int kMaxStagesDev = 16;
-constexpr uint32_t kOperandA = 128 * kBlockK * 2;  // bytes of the MMA A operand per stage
+constexpr uint32_t kOperandA = 128 * kBlockK * 2;  // bytes of one 128-row box of 64 k
 constexpr uint32_t kSwizzleRow = 128;              // bytes per swizzled row
 constexpr uint32_t kAtomBytes = 1024;              // 8 swizzled rows
-constexpr uint32_t kChunkBytes = kBlockK * kSwizzleRow;  // one 64-wide M/N chunk of 64 k-rows
 
 enum : int32_t {
     kErrProducer = 0x11,
@@ -63,6 +62,7 @@ struct __align__(8) Ctrl {
     uint64_t tmem_empty[2];
     uint64_t final_bar;
     uint64_t exch_bar;  // cluster split-K: the peers' partials are ready (rank 0)
+    uint64_t fix_bar[4];  // split-K fixup of a CTA's final item: 64-column units of the partials landed
     uint32_t tmem_addr;
     int32_t abort_flag;
     int32_t last_flag;
@@ -106,9 +106,13 @@ struct ModeTraits {
     // last partial one (0 if none)
     static constexpr uint32_t kBFull = kBCols / 64, kBRem = kBCols % 64;
     static constexpr uint32_t kBChunks = kBFull + (kBRem ? 1 : 0);
-    // k-rows per ring stage (the plan's block_k): the swapped kernel's
-    // small MMAs take 128 per stage, the others 64
-    static constexpr uint32_t kBK = kSwap ? 2 * kBlockK : kBlockK;
+    // k-rows per ring stage (the plan's block_k): 128 (8 MMAs per stage, so
+    // that the MMA warp's fixed per-stage work -- barrier wait, fence,
+    // commit -- is paid once per 8 MMAs), except for the 256-column tiles:
+    // their MMAs already outlast that work, and 64-row stages keep the ring
+    // twice as deep (128 x 256: 128-row stages would leave only two)
+    static constexpr uint32_t kBK = (kMode == 0 || kMode == 3) ? kBlockK : 2 * kBlockK;
+    static constexpr uint32_t kSub = kBK / kBlockK;  // 64-k boxes per stage
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if this CTA is aborting.
@@ -240,31 +244,44 @@ struct Producer {
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
             const int32_t k0 = kb * (int32_t)T::kBK;
+            constexpr uint32_t kBChunk = T::kBK * kSwizzleRow;  // one 64-column chunk of B (K, N)
             if constexpr (T::kPair) {
                 const uint32_t full_leader = mapa_shared(full, 0);
                 if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
-                tma_load_2d_pair(a_dst, tmA, full_leader, k0, a_row);
+#pragma unroll
+                for (uint32_t i = 0; i < T::kSub; ++i)
+                    tma_load_2d_pair(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
                 if (b_nk) {
-                    tma_load_2d_pair(b_dst, tmB, full_leader, k0, b_col);  // this CTA's kBCols rows of B
+                    // this CTA's kBCols rows of B, one K-major box per 64 k
+#pragma unroll
+                    for (uint32_t i = 0; i < T::kSub; ++i)
+                        tma_load_2d_pair(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
+                                         k0 + (int32_t)(i * kBlockK), b_col);
                 } else {
 #pragma unroll
                     for (uint32_t j = 0; j < T::kBFull; ++j)
-                        tma_load_2d_pair(b_dst + j * kChunkBytes, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                        tma_load_2d_pair(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
                     if constexpr (T::kBRem != 0)
-                        tma_load_2d_pair(b_dst + T::kBFull * kChunkBytes, tmB2, full_leader,
+                        tma_load_2d_pair(b_dst + T::kBFull * kBChunk, tmB2, full_leader,
                                          b_col + 64 * (int32_t)T::kBFull, k0);
                 }
             } else {
                 mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
-                    tma_load_2d_maybe_hint(a_dst, tmA, full, k0, a_row, once_a, pol_first);
+#pragma unroll
+                    for (uint32_t i = 0; i < T::kSub; ++i)
+                        tma_load_2d_maybe_hint(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                               once_a, pol_first);
                     if (b_nk) {
-                        // the tile's kBN rows of B, K-major like A
-                        tma_load_2d_maybe_hint(b_dst, tmB, full, k0, b_col, once_b, pol_first);
+                        // the tile's kBN rows of B, K-major like A, one box per 64 k
+#pragma unroll
+                        for (uint32_t i = 0; i < T::kSub; ++i)
+                            tma_load_2d_maybe_hint(b_dst + i * T::kBN * kSwizzleRow, tmB, full,
+                                                   k0 + (int32_t)(i * kBlockK), b_col, once_b, pol_first);
                     } else {
 #pragma unroll
                         for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                            tma_load_2d_maybe_hint(b_dst + j * kChunkBytes, tmB, full, b_col + 64 * (int32_t)j, k0,
+                            tma_load_2d_maybe_hint(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0,
                                                    once_b, pol_first);
                     }
                 } else {
@@ -340,13 +357,17 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
             b_off[k] = (k / 4) * b_box16 + (k % 4) * 2u;
         }
     } else {
+        // A: one 128-row K-major box per 64 k; B (N, K): one box of its rows
+        // per 64 k; B (K, N): 64-column chunks of kBK k-rows
+        constexpr uint32_t kARows16 = kOperandA >> 4;
+        constexpr uint32_t kBRows16 = ((T::kPair ? T::kBCols : T::kBN) * kSwizzleRow) >> 4;
         a_desc0 = make_sw128_desc(stages, 16, kAtomBytes);
         b_desc0 = b_nk ? make_sw128_desc(stages + a_bytes, 16, kAtomBytes)
-                       : make_sw128_desc(stages + a_bytes, kChunkBytes, kAtomBytes);
+                       : make_sw128_desc(stages + a_bytes, T::kBK * kSwizzleRow, kAtomBytes);
 #pragma unroll
         for (uint32_t k = 0; k < kK; ++k) {
-            a_off[k] = k * 2u;
-            b_off[k] = b_nk ? k * 2u : k * kMNStep;
+            a_off[k] = (k / 4) * kARows16 + (k % 4) * 2u;
+            b_off[k] = b_nk ? (k / 4) * kBRows16 + (k % 4) * 2u : k * kMNStep;
         }
     }
     const uint32_t stride16 = stride >> 4;
@@ -473,6 +494,7 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     const uint32_t half = T::kPair ? rank : 0u;      // which 128 rows of a pair tile
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
+    const bool shared_reduction = concurrent_split(pl);
     const int64_t tile_elems = (int64_t)128 * ncols;
     const uint32_t my_staging = staging + quarter * 8192u;  // two 4 KiB buffers per warp
     uint32_t sbuf = 0;
@@ -633,6 +655,101 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
         const int64_t split_id = T::kPair ? (int64_t)w.sk_index * 2 + rank : (int64_t)w.sk_index;
         uint32_t* const counter = p.counters + split_id;
         uint32_t* const flags = p.counters + pl.counter_count + split_id * pl.max_slots;
+        if (shared_reduction) {
+            // Every slot of this tile runs at the same time (at most one split
+            // item per worker), so the reduction is shared: slot s owns
+            // columns [s * own, (s + 1) * own).  Each slot publishes the
+            // columns the others own, waits (bounded) until all others have
+            // published, then sums and stores its own columns.  The last
+            // slot to finish reading resets the counter and flags.
+            const float4* const tbase = reinterpret_cast<const float4*>(ws + split_id * pl.max_slots * tile_elems);
+            const int64_t sq = tile_elems / 4;
+            const uint32_t own = ncols / (uint32_t)w.nslots;
+            const uint32_t own0 = (uint32_t)w.slot * own;
+            float4* const mine = const_cast<float4*>(tbase) + w.slot * sq;
+            for (uint32_t c = 0; c < ncols; c += kChunk) {
+                if (c >= own0 && c < own0 + own) continue;
+                __syncwarp();
+                tmem_load_chunk<kMode>(taddr + c, v);
+#pragma unroll
+                for (int j = 0; j < kQ; ++j)
+                    __stcg(mine + (int64_t)(c / 4 + j) * 128 + lane_row,
+                           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            }
+            named_bar_sync(kEpiBarrier, kEpiThreads);
+            if (threadIdx.x == 64) {
+                __threadfence();  // the partial is visible before the flag
+                atomicExch(flags + w.slot, 1u);
+            }
+            bool ready = true;
+            if (threadIdx.x == 64) {
+                volatile uint32_t* vf = flags;
+                volatile int32_t* abort_flag = &ctrl->abort_flag;
+                const uint64_t t0 = globaltimer_ns();
+                for (int32_t sl = 0; sl < w.nslots && ready; ++sl) {
+                    if (sl == w.slot) continue;
+                    while (vf[sl] == 0u) {
+                        if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                            *abort_flag = 1;
+                            atomicCAS(p.err, 0, kErrEpilogue);
+                            ready = false;
+                            break;
+                        }
+                    }
+                }
+                __threadfence();
+            }
+            ready = named_bar_and(kEpiBarrier, kEpiThreads, ready);
+            if (!ready) {
+                release_tmem();
+                break;
+            }
+            for (uint32_t c = own0; c < own0 + own; c += kChunk) {
+                __syncwarp();
+                tmem_load_chunk<kMode>(taddr + c, v);  // own share
+                float4 acc[kQ];
+#pragma unroll
+                for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4* src = tbase + (int64_t)(c / 4) * 128 + lane_row;
+                for (int32_t sl = 0; sl < w.nslots; ++sl) {
+                    float4 x[kQ];
+                    if (sl == w.slot) {
+#pragma unroll
+                        for (int j = 0; j < kQ; ++j) x[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kQ; ++j) x[j] = __ldcg(src + sl * sq + j * 128);
+                    }
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) {
+                        acc[j].x += x[j].x;
+                        acc[j].y += x[j].y;
+                        acc[j].z += x[j].z;
+                        acc[j].w += x[j].w;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < kQ; ++j) {
+                    v[4 * j] = acc[j].x;
+                    v[4 * j + 1] = acc[j].y;
+                    v[4 * j + 2] = acc[j].z;
+                    v[4 * j + 3] = acc[j].w;
+                }
+                sink(w, c);
+            }
+            release_tmem();
+            named_bar_sync(kEpiBarrier, kEpiThreads);  // this slot has read every partial it needs
+            if (threadIdx.x == 64) {
+                if (atomicAdd(counter, 1u) == (uint32_t)(w.nslots - 1)) {
+                    // every slot is done reading: reset for the next launch
+                    for (int32_t sl = 0; sl < w.nslots; ++sl) flags[sl] = 0u;
+                    __threadfence();
+                    *counter = 0u;
+                }
+            }
+            ++local;
+            continue;
+        }
         named_bar_sync(kEpiBarrier, kEpiThreads);  // last_flag of the previous item is consumed
         if (threadIdx.x == 64) {
             const uint32_t prev = atomicAdd(counter, 1u);
@@ -684,18 +801,54 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
             break;
         }
         __threadfence();
+        // When this is the CTA's final item its ring is idle: fetch the
+        // other slots' partials into it with bulk copies (one per 64-column
+        // unit and slot, all in flight at once) instead of latency-bound
+        // loads from every thread.  The ring must hold them all.
+        const uint32_t part_bytes = ncols * 512u;  // one slot: 128 lanes x ncols fp32
+        bool fast;
+        {
+            WorkIter peek = wi;
+            WorkItem nx;
+            fast = !peek.next(pl, nx) && (uint32_t)(w.nslots - 1) * part_bytes <= staging - stages;
+        }
+        if (fast && threadIdx.x == 64) {
+            fence_proxy_async_global();
+            for (uint32_t u = 0; u * 64u < ncols; ++u) {
+                const uint32_t ub = (ncols - u * 64u < 64u ? ncols - u * 64u : 64u) * 512u;
+                mbar_arrive_expect_tx(smem_u32(&ctrl->fix_bar[u]), (uint32_t)(w.nslots - 1) * ub);
+                uint32_t q = 0;
+                for (int32_t sl = 0; sl < w.nslots; ++sl) {
+                    if (sl == w.slot) continue;
+                    bulk_load(stages + q * part_bytes + u * 64u * 512u,
+                              reinterpret_cast<const char*>(base + sl * slot_q) + u * 64u * 512u, ub,
+                              smem_u32(&ctrl->fix_bar[u]));
+                    ++q;
+                }
+            }
+        }
         for (uint32_t c = 0; c < ncols; c += kChunk) {
+            if (fast && c % 64u == 0) {
+                bool ok = wait_phase(smem_u32(&ctrl->fix_bar[c / 64u]), 0, ctrl, p, kErrEpilogue);
+                if (!named_bar_and(kEpiBarrier, kEpiThreads, ok)) break;
+            }
             __syncwarp();
             tmem_load_chunk<kMode>(taddr + c, v);  // own share
             float4 acc[kQ];
 #pragma unroll
             for (int j = 0; j < kQ; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             const float4* src = base + (int64_t)(c / 4) * 128 + lane_row;
+            uint32_t q = 0;
             for (int32_t sl = 0; sl < w.nslots; ++sl) {
                 float4 x[kQ];
                 if (sl == w.slot) {
 #pragma unroll
                     for (int j = 0; j < kQ; ++j) x[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else if (fast) {
+                    const uint32_t srow = stages + q * part_bytes + (((c / 4) * 128u + lane_row) << 4);
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) x[j] = ld_shared_f4(srow + ((uint32_t)j * 128u << 4));
+                    ++q;
                 } else {
 #pragma unroll
                     for (int j = 0; j < kQ; ++j) x[j] = __ldcg(src + sl * slot_q + j * 128);
@@ -748,8 +901,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMA A operand per stage: 128 rows of 64 k; swapped, one 64-wide chunk
     // of B columns (kBK k-rows) per 64 tile columns (a narrow tile, at most
     // 64 columns, takes one chunk and an M = 64 MMA)
-    const uint32_t a_bytes = T::kSwap ? (pl.tile_n <= 64 ? 1u : 2u) * T::kBK * kSwizzleRow : kOperandA;
-    const uint32_t b_bytes = (T::kPair ? T::kBChunks * kChunkBytes
+    const uint32_t a_bytes = T::kSwap ? (pl.tile_n <= 64 ? 1u : 2u) * T::kBK * kSwizzleRow : T::kSub * kOperandA;
+    const uint32_t b_bytes = (T::kPair ? T::kBChunks * T::kBK * kSwizzleRow
                                        : ((uint32_t)pl.mma_n * T::kBK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -773,6 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctrl->tmem_empty[b]), (T::kPair ? 2u : 1u) * (kEpiThreads / 32));
         }
         mbar_init(smem_u32(&ctrl->final_bar), 1);
+        for (int u = 0; u < 4; ++u) mbar_init(smem_u32(&ctrl->fix_bar[u]), 1);
         // cluster split-K: swapped, the peers push their partials into this
         // CTA's buffer (one local arrival, completed by their bytes); tiled,
         // each peer arrives once its partial sits in its own ring

@@ -17,11 +17,6 @@ constexpr int32_t kSmemLimit = 227 * 1024;  // opt-in shared memory per CTA
 constexpr int32_t kStagingBytes = 32 * 1024;  // C staging for TMA stores (tiled paths)
 constexpr int32_t kMaxStages = 16;
 constexpr int32_t kSwizzleRowBytes = 128;   // one swizzled shared-memory row
-constexpr int32_t kOperandABytes = 128 * kBlockK * 2;  // MMA A operand: 128 rows x 64 k
-// k-rows per stage of the swapped-operand kernel: its MMAs are small
-// (N = padded M), so a stage of 128 k-rows halves the fixed per-stage cost
-// (barrier round trip, MMA commit, TMA issues) per byte streamed
-constexpr int32_t kSwapBlockK = 2 * kBlockK;
 
 // Cost model in microseconds, calibrated against GB300 measurements
 // (sm clock ~1.9-2.1 GHz): per-k-block mainloop time of each kernel shape,
@@ -45,8 +40,8 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     if (path == 4 && mma_n >= 256) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
         c.kb = 0.29;
         c.tile_store = 2.5;
-        c.partial = 6.0;
-        c.reduce_per_slot = 4.0;
+        c.partial = 3.0;           // measured: ~3 us to publish a 128 KiB partial
+        c.reduce_per_slot = 3.0;
     } else if (path == 4 && mma_n == 192) {  // CTA pair, 256 x 192: measured no faster per
         c.kb = 0.32;                          // k-block than 256 x 256 (the MMA warp's loop bounds both)
         c.tile_store = 1.9;
@@ -72,7 +67,10 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
         c.tile_store = 1.3;
         c.partial = 3.0;
         c.reduce_per_slot = 2.0;
-    } else {
+    }
+    // the figures above are per 64 k-rows; stages of 128 k-rows cost twice
+    if ((path == 2 || path == 4) && mma_n < 256) c.kb *= 2.0;
+    if (path == 3) {
         // swapped operands, streaming B: ~0.4 us per 18 KiB stage per SM
         c.kb = 0.40 * stage_bytes / 18432.0;
         c.tile_store = 0.5;
@@ -94,6 +92,7 @@ static double estimate(const gemm_relu_plan_t& p, const Costs& c) {
         WorkIter wi;
         wi.init(p, cta);
         const int32_t dp_n = wi.dp_n;
+        const bool shared = concurrent_split(p);
         double t = c.fill + (double)dp_n * ((double)p.num_kb * c.kb + 0.25 * c.tile_store);
         wi.dp_i = dp_n;  // data-parallel items are costed above
         bool any = dp_n > 0;
@@ -103,6 +102,8 @@ static double estimate(const gemm_relu_plan_t& p, const Costs& c) {
             t += (double)(w.kb1 - w.kb0) * c.kb;
             if (w.nslots == 1)
                 t += 0.25 * c.tile_store;
+            else if (shared)  // publish, read and store (S-1)/S, (S-1)/S and 1/S of the tile
+                t += (c.partial + c.reduce_per_slot) * (w.nslots - 1) / w.nslots + c.tile_store / w.nslots;
             else
                 t += c.partial + (w.slot == 0 ? w.nslots * c.reduce_per_slot + c.tile_store : 0.0);
         }
@@ -167,7 +168,9 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     p.tiles_m = (int32_t)((M + p.tile_m - 1) / p.tile_m);
     p.tiles_n = (int32_t)((N + p.tile_n - 1) / p.tile_n);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.block_k = (path == 3) ? kSwapBlockK : kBlockK;
+    // k-rows per stage: 128, except 256-column tiles (tensor-bound already;
+    // 64-row stages keep their ring deeper)
+    p.block_k = (mma_n == 256 && path != 3) ? kBlockK : 2 * kBlockK;
     p.num_kb = (int32_t)((K + p.block_k - 1) / p.block_k);
     p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
     // per CTA: columns of the MMA B operand it loads (half of the tile for
@@ -178,9 +181,9 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     // 64-wide chunk of B columns per 64 tile columns (a narrow tile, at most
     // 64 columns, takes one chunk and an M = 64 MMA)
     const bool narrow = (path == 3 && p.tile_n <= 64);
-    const int32_t a_region = (path == 3) ? (narrow ? 1 : 2) * p.block_k * kSwizzleRowBytes : kOperandABytes;
+    const int32_t a_region = (path == 3) ? (narrow ? 1 : 2) * p.block_k * kSwizzleRowBytes : 128 * p.block_k * 2;
     // bytes the TMA copies of one stage deliver
-    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * p.block_k * 2 : kOperandABytes;
+    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * p.block_k * 2 : 128 * p.block_k * 2;
     p.stage_bytes = a_box_bytes + b_bytes;
     // B region: a pair CTA's (K, N) chunks are 64 columns wide, the last
     // one possibly partial (256 x 192 tiles: 96 columns = 1.5 chunks)
@@ -258,7 +261,10 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, i
                 for (int32_t sp = 2; sp <= 4 && sp <= p.num_kb; ++sp) {
                     gemm_relu_plan_t q = p;
                     finish_split(q, workers, full * workers, T % workers, sp);
-                    const double cost = estimate(q, c) + 1e-3 * (double)q.sk_tiles;
+                    // (+1.5 us: the fixup's cost varies; take the split tail
+                    // only for a clear gain -- 2048 x 8192 x 2048 measured no
+                    // faster with an estimated 0.5 us gain)
+                    const double cost = estimate(q, c) + 1.5 + 1e-3 * (double)q.sk_tiles;
                     if (best_cost < 0.0 || cost < best_cost) {
                         best_cost = cost;
                         best = q;

@@ -103,6 +103,20 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src,
         : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory (addresses 16-byte
+// aligned, size a multiple of 16); its bytes complete mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Orders this thread's earlier view of global memory (generic proxy) before
+// its later asynchronous-proxy accesses (bulk copies) of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -56,6 +56,15 @@ GR_HD int32_t sk_owner(const gemm_relu_plan_t& p, int64_t x) {
     return (int32_t)(p.sk_r + (x - big) / p.sk_q);
 }
 
+// Split tiles whose slots all run at once (at most one split item per
+// worker) and whose columns divide into whole epilogue chunks per slot:
+// their slots share the reduction (each sums and stores 1/splits of the
+// columns) instead of leaving it all to the last arriver.
+GR_HD bool concurrent_split(const gemm_relu_plan_t& p) {
+    const int32_t chunk = (p.path == 3) ? 16 : 64;  // epilogue chunk (columns)
+    return p.splits > 1 && (int64_t)p.sk_tiles * p.splits <= p.grid && p.mma_n % (p.splits * chunk) == 0;
+}
+
 struct WorkItem {
     int32_t tile;      // linear tile id
     int32_t tm, tn;    // tile row / column
