@@ -949,6 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctrl->tmem_addr;
+    // Everything above touches only this CTA's (or cluster's) on-chip state,
+    // so it may overlap the previous kernel of the stream; nothing below may
+    // read or write global memory before that kernel has completed.  The
+    // next kernel may start launching now: it waits the same way.
+    grid_launch_dependents();
+    grid_dependency_wait();
 
     if (warp == 0) {
         if (lane == 0) {

@@ -201,19 +201,26 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
         d.attr_set[kMode] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)(pl.grid * pl.cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = st;
+    // programmatic dependent launch: this kernel's set-up may overlap the
+    // tail of the previous kernel on the stream (the kernel waits for that
+    // kernel before touching global memory)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n_attr = 1;
     if (pl.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)pl.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)pl.cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n_attr = 2;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
     if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tb2, tc, kp) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;

@@ -139,6 +139,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- launch overlap
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream start launching (its CTAs still wait below before touching
+// memory); wait blocks until the preceding kernel has completed and its
+// memory is visible.  Both are no-ops for a launch without a programmatic
+// dependency.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
