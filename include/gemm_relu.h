@@ -202,8 +202,8 @@ typedef struct {
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
  * "tiled256", "tiled128", "tiled64" (128 x 64 tiles), "swap" (M <= 128 only), "swapnW" (M <= 128,
  * data-parallel tiles W = 8..64 columns wide), "pair" (CTA pairs, 256 x
- * 256 tiles), "pair192" or "pair128" (CTA pairs, 256 x 192 / 256 x 128
- * tiles), optionally
+ * 256 tiles), "pair192", "pair128" or "pair64" (CTA pairs, 256 x 192 /
+ * 256 x 128 / 256 x 64 tiles), optionally
  * followed by ":dp" to forbid splitting tiles along K, by ":sN" to cut
  * every tile into N equal K ranges (the split schedule), or by ":c2" to
  * split every tile's K range between the two CTAs of a cluster, which

@@ -48,7 +48,7 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["mma_n"] in (64, 128, 256) and d["tile_m"] == 128
         assert d["mma_m"] == 128 and (d["cluster"] == 1 or csk)
     else:
-        assert d["mma_n"] in (128, 192, 256)
+        assert d["mma_n"] in (64, 128, 192, 256)
         assert (d["mma_m"], d["tile_m"], d["tile_n"], d["cluster"]) == (256, 256, d["mma_n"], 2)
         assert d["stage_bytes"] == (128 + d["mma_n"] // 2) * d["block_k"] * 2
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
@@ -125,11 +125,12 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
                                    "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3", "swapn56",
                                    "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk",
                                    "tiled128:sk", "pair128", "pair128:dp", "pair128:s3", "tiled64",
-                                   "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2"])
+                                   "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2", "pair64",
+                                   "pair64:s2"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "pair128": (4, 128),
-            "tiled64": (2, 64), "pair192": (4, 192)}
+            "tiled64": (2, 64), "pair192": (4, 192), "pair64": (4, 64)}
     for shape in SHAPES:
         d = _check(gemm_lib, *shape, 152, forced=True)
         if force.startswith("swap"):

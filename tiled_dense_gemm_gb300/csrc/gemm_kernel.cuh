@@ -90,13 +90,14 @@ struct KParams {
 // 256 x 128 (each CTA holds 128 rows of A and 64 columns of B); 5: C tile
 // 128 x 64; 6: CTA pair, C tile 256 x 192 (each CTA holds 96 columns of B:
 // one 64-wide chunk and a half-filled one, whose 32 columns come through a
-// second tensor map of B when B is stored (K, N)).
+// second tensor map of B when B is stored (K, N)); 7: CTA pair, C tile
+// 256 x 64 (each CTA holds 32 columns of B, a half-filled chunk).
 template <int kMode>
 struct ModeTraits {
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6);
+    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6 || kMode == 7);
     static constexpr int kCG = kPair ? 2 : 1;
-    static constexpr uint32_t kBN = (kMode == 5)                   ? 64
+    static constexpr uint32_t kBN = (kMode == 5 || kMode == 7)   ? 64
                                     : (kMode == 1 || kMode == 4) ? 128
                                     : (kMode == 6)               ? 192
                                                                  : 256;  // C columns per tile

@@ -46,7 +46,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[7] = {false, false, false, false, false, false, false};
+    bool attr_set[8] = {false, false, false, false, false, false, false, false};
     std::vector<StreamBuffers> streams;
 };
 
@@ -341,6 +341,7 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     if (pl.path == 4) {
         if (pl.mma_n == 128) return launch_mode<4>(d, pl, kp, ta, tb, tb2, tc, st);
         if (pl.mma_n == 192) return launch_mode<6>(d, pl, kp, ta, tb, tb2, tc, st);
+        if (pl.mma_n == 64) return launch_mode<7>(d, pl, kp, ta, tb, tb2, tc, st);
         return launch_mode<3>(d, pl, kp, ta, tb, tb2, tc, st);
     }
     if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tb2, tc, st);

@@ -47,6 +47,11 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
         c.tile_store = 1.9;
         c.partial = 4.5;
         c.reduce_per_slot = 3.0;
+    } else if (path == 4 && mma_n == 64) {  // CTA pair, 256 x 64 (each CTA 128 x 64): measured
+        c.kb = 0.25;                         // slower than one CTA per 128 x 64 tile
+        c.tile_store = 0.7;
+        c.partial = 1.5;
+        c.reduce_per_slot = 1.0;
     } else if (path == 4) {  // CTA pair, 256 x 128 (each CTA 128 x 128): measured no faster
         c.kb = 0.31;         // per k-block than one CTA per 128 x 128 tile
         c.tile_store = 1.3;
@@ -336,7 +341,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // for 32 < M <= 64 only where it splits K without stream-K (below);
     // else, and above, the 128 x 128 tiled kernel measured faster
     bool want_swap = M <= 64, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
-    bool want_pair128 = want_pair, want_t64 = want_t128, want_pair192 = want_pair;
+    bool want_pair128 = want_pair, want_t64 = want_t128, want_pair192 = want_pair, want_pair64 = false;
     const bool swap_only = M <= 32 || starts_with(f, "swap");
     if (starts_with(f, "swap") && M <= 128) {
         want_t256 = want_t128 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
@@ -350,6 +355,9 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     } else if (starts_with(f, "tiled128")) {
         want_swap = want_t256 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
         want_t128 = true;
+    } else if (starts_with(f, "pair64") && pairs > 0) {
+        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair128 = want_pair192 = false;
+        want_pair64 = true;
     } else if (starts_with(f, "pair192") && pairs > 0) {
         want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair128 = false;
         want_pair192 = true;
@@ -445,6 +453,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     if (want_pair) take(4, 256, pairs);
     if (want_pair128) take(4, 128, pairs);
     if (want_pair192) take(4, 192, pairs);
+    if (want_pair64) take(4, 64, pairs);
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
     if (want_t64) take(2, 64, num_sms);
