@@ -189,6 +189,9 @@ typedef struct {
     int32_t stage_bytes; /* bytes of A and B tile per ring stage */
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
+    int32_t pack;        /* 1: before the GEMM, copy each operand whose row pitch is not a
+                            multiple of 128 bytes to a 128-byte pitch (library workspace);
+                            only when forced (":pk"), as it measured slower */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
     int64_t counter_count;   /* arrival counters (one per split tile and CTA of a worker); the
                                 counter array also holds max_slots ready flags per counter */
@@ -209,7 +212,8 @@ typedef struct {
  * split every tile's K range between the two CTAs of a cluster, which
  * combine their halves through distributed shared memory ("pair" has no
  * ":c2": its cluster already holds one 256-row tile), or by ":sk" to run
- * every tile stream-K over all workers.
+ * every tile stream-K over all workers; ":pk" / ":npk" force / forbid the
+ * packing of misaligned operands.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);

@@ -282,7 +282,8 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
                                    "swap:sk", "tiled128:sk", "pair128", "pair128:dp", "pair128:s3",
                                    "tiled64", "tiled64:s3", "tiled64:c2", "pair192", "pair192:s3",
                                    "tiled128:s2", "pair:s2", "pair:s4", "tiled256:s2", "tiled64:s2",
-                                   "pair64", "pair64:s2"])
+                                   "pair64", "pair64:s2", "tiled128:pk", "pair:pk",
+                                   "tiled64:pk", "pair:t2:pk"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands with 128-wide or narrow tiles), with and without

@@ -56,6 +56,7 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     assert d["block_k"] == (64 if (d["path"] in (2, 4) and d["mma_n"] == 256) else 128)
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
+    assert d["pack"] in (0, 1) and (d["pack"] == 0 or d["path"] in (2, 4))
     assert d["smem_bytes"] <= SMEM_LIMIT
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
     assert 1 <= d["grid"] * d["cluster"] <= sms
@@ -161,6 +162,19 @@ def test_tail_wave_split(gemm_lib, monkeypatch, force, sp):
         if T % workers:
             assert d["dp_tiles"] == (T // workers) * workers
             assert d["sk_tiles"] == T % workers and d["splits"] == sp and d["max_slots"] == sp
+
+
+def test_packing_decision(gemm_lib, monkeypatch):
+    monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
+    # only when forced (measured no faster on the ragged workload)
+    assert gemm_lib.plan(3000, 5000, 2056, 152).pack == 0
+    assert gemm_lib.plan(4096, 4096, 4096, 152).pack == 0
+    assert gemm_lib.plan(300, 264, 2056, 152).pack == 0
+    assert gemm_lib.plan(16, 8192, 8200, 152).pack == 0
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "tiled128:pk")
+    assert gemm_lib.plan(300, 264, 2056, 152).pack == 1
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "pair:npk")
+    assert gemm_lib.plan(3000, 5000, 2056, 152).pack == 0
 
 
 def test_random_shapes(gemm_lib):

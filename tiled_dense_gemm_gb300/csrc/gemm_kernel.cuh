@@ -259,9 +259,11 @@ struct Producer {
                         tma_load_2d_pair(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
                                          k0 + (int32_t)(i * kBlockK), b_col);
                 } else {
+                    if constexpr (T::kBFull > 0) {
 #pragma unroll
-                    for (uint32_t j = 0; j < T::kBFull; ++j)
-                        tma_load_2d_pair(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                        for (uint32_t j = 0; j < T::kBFull; ++j)
+                            tma_load_2d_pair(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                    }
                     if constexpr (T::kBRem != 0)
                         tma_load_2d_pair(b_dst + T::kBFull * kBChunk, tmB2, full_leader,
                                          b_col + 64 * (int32_t)T::kBFull, k0);

@@ -17,6 +17,25 @@
 namespace gr {
 
 // C := +0 for K == 0 (the empty sum).
+// Copy of an operand's rows to a 128-byte-aligned row pitch (16-byte
+// vectors; pitches in vectors).  blockIdx.y selects the operand.
+struct PackJob {
+    const uint4* src;
+    uint4* dst;
+    int64_t rows, row_vecs, src_pitch, dst_pitch;
+};
+
+__global__ void pack_rows_kernel(PackJob a, PackJob b) {
+    grid_launch_dependents();
+    grid_dependency_wait();  // the operands may come from the previous kernel
+    const PackJob& j = blockIdx.y == 0 ? a : b;
+    for (int64_t r = blockIdx.x; r < j.rows; r += gridDim.x) {
+        const uint4* src = j.src + r * j.src_pitch;
+        uint4* dst = j.dst + r * j.dst_pitch;
+        for (int64_t c = threadIdx.x; c < j.row_vecs; c += blockDim.x) dst[c] = src[c];
+    }
+}
+
 __global__ void zero_fill_kernel(uint4* c, int64_t n16) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
@@ -34,6 +53,8 @@ struct StreamBuffers {
     size_t ws_bytes = 0;
     uint32_t* counters = nullptr;  // split-K arrival counters + ready flags (zero between launches)
     size_t counter_bytes = 0;
+    void* packed = nullptr;  // operands copied to a 128-byte row pitch
+    size_t packed_bytes = 0;
     void* hA = nullptr;  // staging for the host-buffer entry point
     void* hB = nullptr;
     void* hC = nullptr;
@@ -175,9 +196,9 @@ int grow(void** buf, size_t* have, size_t need, cudaStream_t stream, bool zero) 
 }
 
 int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool bf16) {
+              uint32_t box_outer, bool bf16, uint64_t pitch_elems = 0) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};  // bytes between rows
+    cuuint64_t strides[1] = {(pitch_elems ? pitch_elems : inner) * 2};  // bytes between rows
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -299,30 +320,71 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         kp.ws = sb.ws;
         kp.counters = sb.counters;
     }
+    // operands whose row pitch is not a multiple of 128 bytes: copy them to
+    // a 128-byte pitch first when the plan says it pays
+    uint64_t a_pitch = 0, b_pitch = 0;  // elements; 0 = as stored
+    if (pl.pack) {
+        const uint64_t b_rows = b_nk ? (uint64_t)N : (uint64_t)K, b_len = b_nk ? (uint64_t)K : (uint64_t)N;
+        const bool pa = (K % 64) != 0, pb = (b_len % 64) != 0;
+        if (pa || pb) {
+            const uint64_t ap = ((uint64_t)K + 63) / 64 * 64, bp = (b_len + 63) / 64 * 64;
+            const size_t a_bytes = pa ? (size_t)M * ap * 2 : 0, b_bytes = pb ? (size_t)b_rows * bp * 2 : 0;
+            StreamBuffers& sb = buffers_for_locked(d, st);
+            int rc = grow(&sb.packed, &sb.packed_bytes, a_bytes + b_bytes, st, false);
+            if (rc != GEMM_OK) return rc;
+            uint8_t* pbuf = static_cast<uint8_t*>(sb.packed);
+            PackJob ja = {reinterpret_cast<const uint4*>(A), reinterpret_cast<uint4*>(pbuf), pa ? M : 0,
+                          (int64_t)K / 8, (int64_t)K / 8, (int64_t)ap / 8};
+            PackJob jb = {reinterpret_cast<const uint4*>(B), reinterpret_cast<uint4*>(pbuf + a_bytes),
+                          pb ? (int64_t)b_rows : 0, (int64_t)b_len / 8, (int64_t)b_len / 8, (int64_t)bp / 8};
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            const int64_t most = pa && pb ? (M > (int64_t)b_rows ? M : (int64_t)b_rows) : (pa ? M : (int64_t)b_rows);
+            cfg.gridDim = dim3((unsigned)(most < (int64_t)d.sm_count * 8 ? most : (int64_t)d.sm_count * 8), 2, 1);
+            cfg.blockDim = dim3(256, 1, 1);
+            cfg.stream = st;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cfg, pack_rows_kernel, ja, jb) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+            if (pa) {
+                A = pbuf;
+                a_pitch = ap;
+            }
+            if (pb) {
+                B = pbuf + a_bytes;
+                b_pitch = bp;
+            }
+        }
+    }
     CUtensorMap ta, tb;
     const bool swap = (pl.path == 3);
     // the swapped kernel's exchange buffer holds one peer's partial
     if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
-    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16);
+    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16, a_pitch);
     if (rc != GEMM_OK) return rc;
     CUtensorMap tb2;
     if (!b_nk) {
         // B (K, N): 64-column boxes of one stage's block_k k-rows (a narrow
         // swapped tile: one box of tile_n columns)
         rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
-                       (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k, bf16);
+                       (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k, bf16, b_pitch);
         // a pair CTA whose B columns end in a partial chunk (256 x 192
         // tiles: 96 columns) loads that chunk with narrower boxes
         const uint32_t rem = (pl.path == 4) ? (uint32_t)(pl.mma_n / 2) % 64u : 0u;
         if (rc == GEMM_OK && rem)
-            rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, rem, (uint32_t)pl.block_k, bf16);
+            rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, rem, (uint32_t)pl.block_k, bf16, b_pitch);
         else
             tb2 = tb;
     } else {
         // B (N, K): boxes of 64 k by the rows of N one CTA loads per stage
         const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
                                    : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-        rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16);
+        rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16, b_pitch);
         tb2 = tb;
     }
     if (rc != GEMM_OK) return rc;
@@ -465,6 +527,7 @@ extern "C" void gemm_relu_shutdown(void) {
             for (auto& s : d.streams) {
                 cudaFree(s.ws);
                 cudaFree(s.counters);
+                cudaFree(s.packed);
                 cudaFree(s.hA);
                 cudaFree(s.hB);
                 cudaFree(s.hC);

@@ -450,6 +450,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         }
         if (swap_only) take(3, mpad, num_sms);
     }
+    // (packing is decided after the kernel shape, below)
     if (want_pair) take(4, 256, pairs);
     if (want_pair128) take(4, 128, pairs);
     if (want_pair192) take(4, 192, pairs);
@@ -457,6 +458,15 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
     if (want_t64) take(2, 64, num_sms);
+    // An operand row pitch that is not a multiple of 128 bytes makes every
+    // 128-byte TMA box row straddle two L2 lines (on 3000 x 5000 x 2056 the
+    // L2 served 1.8 sectors per request instead of 3.9, and the GEMM took
+    // 57.5 us against 46.5 for 3072 x 5120 x 2048).  Copying the operands to
+    // a 128-byte pitch first measured slower all the same (59.8 us; the copy
+    // moves 66 MB), so it is only done when forced (":pk").  (The swapped
+    // kernel streams B once: a copy would triple its traffic.)
+    plan->pack = 0;
+    if (contains(f, ":pk") && !contains(f, ":npk") && (plan->path == 2 || plan->path == 4)) plan->pack = 1;
     return GEMM_OK;
 }
 
