@@ -222,7 +222,33 @@ struct Producer {
 
     // Issue up to `budget` k-blocks of copies (all remaining if < 0).
     // Returns false if the CTA is aborting.
-    __device__ __forceinline__ bool issue(int32_t budget) {
+    __device__ __forceinline__ bool issue(int32_t budget) { return run<false>(budget); }
+
+    // L2 prefetches of the boxes of the next `budget` k-blocks, with no
+    // barrier and no copy: safe before the previous kernel of the stream
+    // has finished (a prefetch returns nothing; lines written meanwhile are
+    // current in L2).  Call it on a copy: it advances the position.
+    __device__ __forceinline__ void prefetch(int32_t budget) { run<true>(budget); }
+
+    template <bool kPre>
+    __device__ __forceinline__ void ld_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y) {
+        if constexpr (kPre)
+            tma_prefetch_2d(m, x, y);
+        else
+            tma_load_2d_pair(dst, m, bar, x, y);
+    }
+
+    template <bool kPre>
+    __device__ __forceinline__ void ld(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y,
+                                       bool hinted) {
+        if constexpr (kPre)
+            tma_prefetch_2d(m, x, y);
+        else
+            tma_load_2d_maybe_hint(dst, m, bar, x, y, hinted, pol_first);
+    }
+
+    template <bool kPre>
+    __device__ __forceinline__ bool run(int32_t budget) {
         while (budget != 0) {
             if (!have_item || kb == w.kb1) {
                 if (!wi.next(pl, w)) return true;
@@ -240,7 +266,8 @@ struct Producer {
                     b_col = w.tn * pl.tile_n;
                 }
             }
-            if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return false;
+            if constexpr (!kPre)
+                if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return false;
             const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
@@ -248,44 +275,44 @@ struct Producer {
             constexpr uint32_t kBChunk = T::kBK * kSwizzleRow;  // one 64-column chunk of B (K, N)
             if constexpr (T::kPair) {
                 const uint32_t full_leader = mapa_shared(full, 0);
-                if (rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
+                if (!kPre && rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
 #pragma unroll
                 for (uint32_t i = 0; i < T::kSub; ++i)
-                    tma_load_2d_pair(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
+                    ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
                 if (b_nk) {
                     // this CTA's kBCols rows of B, one K-major box per 64 k
 #pragma unroll
                     for (uint32_t i = 0; i < T::kSub; ++i)
-                        tma_load_2d_pair(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
-                                         k0 + (int32_t)(i * kBlockK), b_col);
+                        ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
+                                      k0 + (int32_t)(i * kBlockK), b_col);
                 } else {
                     if constexpr (T::kBFull > 0) {
 #pragma unroll
                         for (uint32_t j = 0; j < T::kBFull; ++j)
-                            tma_load_2d_pair(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                            ld_pair<kPre>(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
                     }
                     if constexpr (T::kBRem != 0)
-                        tma_load_2d_pair(b_dst + T::kBFull * kBChunk, tmB2, full_leader,
-                                         b_col + 64 * (int32_t)T::kBFull, k0);
+                        ld_pair<kPre>(b_dst + T::kBFull * kBChunk, tmB2, full_leader,
+                                      b_col + 64 * (int32_t)T::kBFull, k0);
                 }
             } else {
-                mbar_arrive_expect_tx(full, tx_bytes);
+                if constexpr (!kPre) mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
 #pragma unroll
                     for (uint32_t i = 0; i < T::kSub; ++i)
-                        tma_load_2d_maybe_hint(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                               once_a, pol_first);
+                        ld<kPre>(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                 once_a);
                     if (b_nk) {
                         // the tile's kBN rows of B, K-major like A, one box per 64 k
 #pragma unroll
                         for (uint32_t i = 0; i < T::kSub; ++i)
-                            tma_load_2d_maybe_hint(b_dst + i * T::kBN * kSwizzleRow, tmB, full,
-                                                   k0 + (int32_t)(i * kBlockK), b_col, once_b, pol_first);
+                            ld<kPre>(b_dst + i * T::kBN * kSwizzleRow, tmB, full,
+                                     k0 + (int32_t)(i * kBlockK), b_col, once_b);
                     } else {
 #pragma unroll
                         for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                            tma_load_2d_maybe_hint(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0,
-                                                   once_b, pol_first);
+                            ld<kPre>(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0,
+                                     once_b);
                     }
                 } else {
                     // MMA A operand: the tile's columns of B, one 64-wide chunk
@@ -297,19 +324,18 @@ struct Producer {
                         // per 64 k
 #pragma unroll
                         for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                            tma_load_2d_maybe_hint(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK),
-                                                   b_col, once_b, pol_first);
+                            ld<kPre>(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK),
+                                     b_col, once_b);
                     } else {
-                        tma_load_2d_maybe_hint(a_dst, tmB, full, b_col, k0, once_b, pol_first);
+                        ld<kPre>(a_dst, tmB, full, b_col, k0, once_b);
                         if (pl.tile_n > 64)
-                            tma_load_2d_maybe_hint(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b,
-                                                   pol_first);
+                            ld<kPre>(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b);
                     }
                     // MMA B operand: the (padded) rows of A, one box per 64 k
 #pragma unroll
                     for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                        tma_load_2d_maybe_hint(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                               once_a, pol_first);
+                        ld<kPre>(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                 once_a);
                 }
             }
             if (++s == S) {
@@ -937,6 +963,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
         fence_mbar_init();
+        if constexpr (T::kSwap) {
+            // The small-M kernel streams B from DRAM: warm L2 with this CTA's
+            // first ring's worth of boxes while the previous kernel finishes
+            // (see Producer::prefetch).  (The tiled kernels read mostly L2-
+            // resident operands: there the extra issue work measured slower.)
+            Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
+            pre.prefetch(pl.num_stages);
+        }
         if (T::kSwap && cluster_split(pl) && rank == 0)
             mbar_arrive_expect_tx(smem_u32(&ctrl->exch_bar),
                                   ((uint32_t)pl.cluster - 1u) * (uint32_t)pl.mma_n * 128u * 4u);

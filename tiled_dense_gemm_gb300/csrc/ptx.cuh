@@ -93,6 +93,15 @@ __device__ __forceinline__ void tma_load_2d_maybe_hint(uint32_t dst, const CUten
         tma_load_2d(dst, m, bar, x, y);
 }
 
+// L2 prefetch of the same box a tma_load_2d at (x, y) would copy: warms L2
+// only, returns nothing to the program.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled copy shared -> global (bulk-group completion).  Elements outside
 // the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x, int32_t y) {
