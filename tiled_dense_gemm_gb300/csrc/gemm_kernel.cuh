@@ -963,14 +963,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
         fence_mbar_init();
-        if constexpr (T::kSwap) {
-            // The small-M kernel streams B from DRAM: warm L2 with this CTA's
-            // first ring's worth of boxes while the previous kernel finishes
-            // (see Producer::prefetch).  (The tiled kernels read mostly L2-
-            // resident operands: there the extra issue work measured slower.)
-            Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
-            pre.prefetch(pl.num_stages);
-        }
+
         if (T::kSwap && cluster_split(pl) && rank == 0)
             mbar_arrive_expect_tx(smem_u32(&ctrl->exch_bar),
                                   ((uint32_t)pl.cluster - 1u) * (uint32_t)pl.mma_n * 128u * 4u);
@@ -991,6 +984,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // read or write global memory before that kernel has completed.  The
     // next kernel may start launching now: it waits the same way.
     grid_launch_dependents();
+    if (warp == 2 && lane == 0) {
+        // Warm L2 with the boxes of this CTA's first k-blocks (two rings'
+        // worth for the small-M kernel, which streams B from DRAM) while the
+        // previous kernel finishes: an idle epilogue warp issues the
+        // prefetches, so the producer is not held up (see Producer::prefetch).
+        Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
+        pre.prefetch((T::kSwap ? 2 : 1) * pl.num_stages);
+    }
     grid_dependency_wait();
 
     if (warp == 0) {
