@@ -192,6 +192,10 @@ typedef struct {
     int32_t pack;        /* 1: before the GEMM, copy each operand whose row pitch is not a
                             multiple of 128 bytes to a 128-byte pitch (library workspace);
                             only when forced (":pk"), as it measured slower */
+    int32_t mcast;       /* 1, or 2: path 2 with 128 x 64 or 128 x 128 tiles, data-parallel only,
+                            launched in clusters of 2 CTAs that take the two column-neighbour
+                            tiles of one tile row; each CTA loads half of every A stage and
+                            the TMA multicasts it into both CTAs */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
     int64_t counter_count;   /* arrival counters (one per split tile and CTA of a worker); the
                                 counter array also holds max_slots ready flags per counter */

@@ -283,7 +283,8 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
                                    "tiled64", "tiled64:s3", "tiled64:c2", "pair192", "pair192:s3",
                                    "tiled128:s2", "pair:s2", "pair:s4", "tiled256:s2", "tiled64:s2",
                                    "pair64", "pair64:s2", "tiled128:pk", "pair:pk",
-                                   "tiled64:pk", "pair:t2:pk"])
+                                   "tiled64:pk", "pair:t2:pk", "tiled128:no3d", "pair:no3d",
+                                   "swap:no3d", "tiled256:no3d", "pair128:no3d"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands with 128-wide or narrow tiles), with and without
@@ -296,3 +297,28 @@ def test_each_kernel_shape_parity(monkeypatch, force):
             ref = oracle.gemm_relu(A, B, relu, threads=THREADS)
             assert_close(C, ref, f"{force} {M}x{N}x{K} relu={relu}")
             assert_relu_sign(C, relu)
+
+
+MCAST_SHAPES = [(1024, 1024, 1024), (2048, 2048, 520), (1100, 2048, 520), (4000, 2000, 136),
+                (8, 4864, 1024), (48, 6144, 2048)]
+
+
+@pytest.mark.parametrize("force", ["tiled64:mc", "tiled128:mc"])
+def test_a_multicast_parity(monkeypatch, force):
+    """Clusters of two CTAs on the two tiles of a column pair, each fetching
+    half of every A stage for both: ragged M, N and K tails, one and
+    several tiles per CTA."""
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    ran = 0
+    for M, N, K in MCAST_SHAPES:
+        if binding.plan(M, N, K, sms).mcast != 2:
+            continue
+        ran += 1
+        A, B = make_inputs(M, N, K, seed=M + 2 * N + K, dist_a="uniform", dist_b="uniform")
+        for relu in (True, False):
+            C = gpu_run(A, B, relu)
+            ref = oracle.gemm_relu(A, B, relu, threads=THREADS)
+            assert_close(C, ref, f"{force} {M}x{N}x{K} relu={relu}")
+            assert_relu_sign(C, relu)
+    assert ran >= 4

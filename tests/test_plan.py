@@ -57,6 +57,11 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
     assert d["pack"] in (0, 1) and (d["pack"] == 0 or d["path"] in (2, 4))
+    assert d["mcast"] in (1, 2)
+    if d["mcast"] == 2:
+        assert d["path"] == 2 and d["mma_n"] in (64, 128) and d["block_k"] == 128 and d["cluster"] == 1
+        assert d["tiles_n"] % 2 == 0 and d["grid"] % 2 == 0
+        assert d["dp_tiles"] == d["num_tiles"] and d["sk_tiles"] == 0 and d["splits"] <= 1
     assert d["smem_bytes"] <= SMEM_LIMIT
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
     assert 1 <= d["grid"] * d["cluster"] <= sms
@@ -94,6 +99,14 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
                 slots[it["tile"]][it["slot"]] = (it["kb0"], it["kb1"], it["nslots"])
         if d["sk_tiles"]:
             sk_units.append(units)
+        if d["mcast"] == 2 and cta % 2 == 1:
+            # the two CTAs of an A-multicast cluster walk the same tile rows
+            # and K ranges in lockstep, on the two tiles of a column pair
+            prev = gemm_lib.plan_work_items(p, cta - 1)
+            assert len(prev) == len(items)
+            for a, b in zip(prev, items):
+                assert a["tm"] == b["tm"] and (a["kb0"], a["kb1"]) == (b["kb0"], b["kb1"])
+                assert a["tn"] % 2 == 0 and b["tn"] == a["tn"] + 1
     # every unit exactly once
     assert len(cover) == d["num_tiles"] * d["num_kb"]
     assert set(cover.values()) == {1}
@@ -127,7 +140,8 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
                                    "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk",
                                    "tiled128:sk", "pair128", "pair128:dp", "pair128:s3", "tiled64",
                                    "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2", "pair64",
-                                   "pair64:s2"])
+                                   "pair64:s2", "tiled64:mc", "tiled128:mc", "tiled256:mc",
+                                   "tiled64:mc:s3", "tiled128:mc:c2"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "pair128": (4, 128),
@@ -140,6 +154,14 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert (d["path"], d["mma_n"]) == want[force.split(":")[0]]
         if force.endswith(":dp"):
             assert d["sk_tiles"] == 0
+        if ":mc" not in force:
+            assert d["mcast"] == 1
+        elif force in ("tiled64:mc", "tiled128:mc"):
+            # every data-parallel plan with an even number of tile columns
+            assert d["mcast"] == (2 if d["tiles_n"] % 2 == 0 and d["dp_tiles"] == d["num_tiles"]
+                                  and d["grid"] % 2 == 0 and d["cluster"] == 1 else 1)
+        else:
+            assert d["mcast"] == 1 or (d["sk_tiles"] == 0 and d["cluster"] == 1)
         if ":c2" in force and d["num_tiles"] <= 76 and d["num_kb"] >= 2:
             assert d["cluster"] == 2 and d["grid"] == d["num_tiles"]
         if force.endswith(":sk"):

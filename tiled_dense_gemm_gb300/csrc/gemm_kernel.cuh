@@ -53,6 +53,7 @@ enum : int32_t {
     kErrMmaAccum = 0x22,
     kErrEpilogue = 0x31,
     kErrFinal = 0x41,
+    kErrConfig = 0x51,
 };
 
 struct __align__(8) Ctrl {
@@ -75,6 +76,10 @@ struct KParams {
     int32_t apply_relu;
     int32_t b_kmajor;     // B stored (N, K) row-major (C = ReLU(A . B^T)) instead of (K, N)
     int32_t out_bf16;     // elements are bfloat16 (inputs and C) instead of binary16
+    // 3-D tensor maps (64-element column blocks as a third dimension): one
+    // copy fetches all 64-k blocks of a stage's A rows (a3d), or all
+    // 64-column chunks / 64-k blocks of its B (b3d), instead of one copy each
+    int32_t a3d, b3d;
     uint32_t idesc;
     uint64_t timeout_ns;
     uint16_t* C;          // 16-bit words of C (binary16 or bfloat16)
@@ -199,6 +204,8 @@ struct Producer {
     uint32_t a_sub_bytes;  // swapped: bytes of one 64-k box of A's padded rows
     bool b_nk;             // B stored (N, K): its boxes are (64 k) x (rows of N)
     uint32_t b_sub_bytes;  // swapped, B stored (N, K): bytes of one 64-k box of the tile's B rows
+    bool mc;               // A multicast: this CTA fetches box `rank` of each A stage for both CTAs
+    bool a3d, b3d;         // one 3-D copy per operand and stage (see KParams)
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
@@ -216,6 +223,9 @@ struct Producer {
         b_sub_bytes = (pl.tile_n <= 64 ? 64u : 128u) * kSwizzleRow;
         once_a = pl.tiles_n == 1;
         once_b = pl.tiles_m == 1;
+        mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
+        a3d = p_.a3d != 0;
+        b3d = p_.b3d != 0;
         pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
     }
@@ -247,6 +257,32 @@ struct Producer {
             tma_load_2d_maybe_hint(dst, m, bar, x, y, hinted, pol_first);
     }
 
+    // 3-D copies at column block 0: (row or k, block)
+    template <bool kPre>
+    __device__ __forceinline__ void ld3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t y, int32_t z,
+                                        bool hinted) {
+        if constexpr (kPre)
+            tma_prefetch_3d(m, 0, y, z);
+        else
+            tma_load_3d_maybe_hint(dst, m, bar, 0, y, z, hinted, pol_first);
+    }
+
+    template <bool kPre>
+    __device__ __forceinline__ void ld3_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t y, int32_t z) {
+        if constexpr (kPre)
+            tma_prefetch_3d(m, 0, y, z);
+        else
+            tma_load_3d_pair(dst, m, bar, 0, y, z);
+    }
+
+    template <bool kPre>
+    __device__ __forceinline__ void ld_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y) {
+        if constexpr (kPre)
+            tma_prefetch_2d(m, x, y);
+        else
+            tma_load_2d_mcast(dst, m, bar, x, y, 0x3);
+    }
+
     template <bool kPre>
     __device__ __forceinline__ bool run(int32_t budget) {
         while (budget != 0) {
@@ -276,15 +312,26 @@ struct Producer {
             if constexpr (T::kPair) {
                 const uint32_t full_leader = mapa_shared(full, 0);
                 if (!kPre && rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
-#pragma unroll
-                for (uint32_t i = 0; i < T::kSub; ++i)
-                    ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
-                if (b_nk) {
-                    // this CTA's kBCols rows of B, one K-major box per 64 k
+                if (a3d) {
+                    ld3_pair<kPre>(a_dst, tmA, full_leader, a_row, k0 / kBlockK);
+                } else {
 #pragma unroll
                     for (uint32_t i = 0; i < T::kSub; ++i)
-                        ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
-                                      k0 + (int32_t)(i * kBlockK), b_col);
+                        ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
+                }
+                if (b_nk) {
+                    // this CTA's kBCols rows of B, one K-major box per 64 k
+                    if (b3d) {
+                        ld3_pair<kPre>(b_dst, tmB, full_leader, b_col, k0 / kBlockK);
+                    } else {
+#pragma unroll
+                        for (uint32_t i = 0; i < T::kSub; ++i)
+                            ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
+                                          k0 + (int32_t)(i * kBlockK), b_col);
+                    }
+                } else if (T::kBRem == 0 && b3d) {
+                    // all of this CTA's 64-column chunks in one copy
+                    ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
                 } else {
                     if constexpr (T::kBFull > 0) {
 #pragma unroll
@@ -298,16 +345,29 @@ struct Producer {
             } else {
                 if constexpr (!kPre) mbar_arrive_expect_tx(full, tx_bytes);
                 if constexpr (!T::kSwap) {
+                    if (T::kSub == 2 && mc) {
+                        // one of the stage's two A boxes; the peer fetches the
+                        // other, and each lands in both CTAs
+                        ld_mc<kPre>(a_dst + rank * kOperandA, tmA, full, k0 + (int32_t)(rank * kBlockK), a_row);
+                    } else if (a3d) {
+                        ld3<kPre>(a_dst, tmA, full, a_row, k0 / kBlockK, once_a);
+                    } else {
 #pragma unroll
-                    for (uint32_t i = 0; i < T::kSub; ++i)
-                        ld<kPre>(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                 once_a);
-                    if (b_nk) {
+                        for (uint32_t i = 0; i < T::kSub; ++i)
+                            ld<kPre>(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                     once_a);
+                    }
+                    if (b_nk && b3d) {
+                        ld3<kPre>(b_dst, tmB, full, b_col, k0 / kBlockK, once_b);
+                    } else if (b_nk) {
                         // the tile's kBN rows of B, K-major like A, one box per 64 k
 #pragma unroll
                         for (uint32_t i = 0; i < T::kSub; ++i)
                             ld<kPre>(b_dst + i * T::kBN * kSwizzleRow, tmB, full,
                                      k0 + (int32_t)(i * kBlockK), b_col, once_b);
+                    } else if (b3d) {
+                        // all of the tile's 64-column chunks in one copy
+                        ld3<kPre>(b_dst, tmB, full, k0, b_col / 64, once_b);
                     } else {
 #pragma unroll
                         for (uint32_t j = 0; j < T::kBN / 64; ++j)
@@ -319,7 +379,14 @@ struct Producer {
                     // of kBK k-rows per TMA box (a narrow tile fills part of
                     // one chunk)
                     constexpr uint32_t kSwapChunk = T::kBK * kSwizzleRow;
-                    if (b_nk) {
+                    if (b3d) {
+                        // one copy: the tile's B rows (B stored (N, K)) for
+                        // every 64 k, or both 64-column chunks (B (K, N))
+                        if (b_nk)
+                            ld3<kPre>(a_dst, tmB, full, b_col, k0 / kBlockK, once_b);
+                        else
+                            ld3<kPre>(a_dst, tmB, full, k0, b_col / 64, once_b);
+                    } else if (b_nk) {
                         // B stored (N, K): the tile's B rows, one K-major box
                         // per 64 k
 #pragma unroll
@@ -332,10 +399,14 @@ struct Producer {
                             ld<kPre>(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b);
                     }
                     // MMA B operand: the (padded) rows of A, one box per 64 k
+                    if (a3d) {
+                        ld3<kPre>(b_dst, tmA, full, a_row, k0 / kBlockK, once_a);
+                    } else {
 #pragma unroll
-                    for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                        ld<kPre>(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                 once_a);
+                        for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
+                            ld<kPre>(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
+                                     once_a);
+                    }
                 }
             }
             if (++s == S) {
@@ -400,6 +471,7 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
         }
     }
     const uint32_t stride16 = stride >> 4;
+    const bool mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
     WorkIter wi;
     wi.init(pl, worker, (int32_t)rank);
     WorkItem w;
@@ -419,8 +491,12 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
 #pragma unroll
             for (uint32_t k = 0; k < kK; ++k)
                 mma_f16_ss<T::kCG>(d_tmem, a_desc + a_off[k], b_desc + b_off[k], idesc, k > 0 ? 1u : acc);
-            // stage free (in both CTAs of a pair) once these MMAs are done
-            mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
+            // stage free (in both CTAs of a pair, or of an A-multicast
+            // cluster, whose peer writes into this stage) once these MMAs are done
+            if (mc)
+                mma_commit_mcast(empty0 + 8u * s, 0x3);
+            else
+                mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -935,10 +1011,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : ((uint32_t)pl.mma_n * T::kBK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // CTA pairs (one MMA for two CTAs) and cluster split-K run in clusters
-    const bool clustered = T::kPair || cluster_split(pl);
+    // CTA pairs (one MMA for two CTAs), cluster split-K and A multicast run
+    // in clusters
+    const bool mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
+    const bool clustered = T::kPair || cluster_split(pl) || mc;
     const uint32_t rank = clustered ? cluster_ctarank() : 0u;
     const int32_t worker = clustered ? (int32_t)(blockIdx.x / (uint32_t)pl.cluster) : (int32_t)blockIdx.x;
+    // A 3-D tensor map must only meet the 3-D copies issued for it: B (K, N)
+    // as whole 64-column chunks (no partial chunk per CTA), a swapped tile
+    // 128 columns wide, and no A multicast (its copies are 2-D).  Every CTA
+    // decides alike, before any barrier.
+    if ((p.b3d && ((!p.b_kmajor && T::kBRem != 0) || (T::kSwap && pl.tile_n != 128))) || (p.a3d && mc)) {
+        if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrConfig);
+        return;
+    }
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -947,7 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!T::kSwap) tma_prefetch_desc(&tmC);
         for (int s = 0; s < pl.num_stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
-            mbar_init(smem_u32(&ctrl->empty[s]), 1);
+            // A multicast: both CTAs' MMAs free a stage (the peer writes into it)
+            mbar_init(smem_u32(&ctrl->empty[s]), mc ? 2u : 1u);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);

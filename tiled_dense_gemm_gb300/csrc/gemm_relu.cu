@@ -209,6 +209,27 @@ int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
 }
 
+// 3-D view of a row-major matrix whose rows hold `inner` elements (a
+// multiple of 64): dimension 0 is 64 elements of a column block, 1 the rows
+// (`outer`, `pitch_elems` apart), 2 the inner / 64 column blocks (128 bytes
+// apart).  A box of `box_blocks` blocks lands block after block in shared
+// memory, each one 128B-swizzled like a 2-D box of the same rows.  The
+// column blocks never reach past a row's end, so every element read is
+// inside the matrix; rows and blocks beyond it read as zero.
+int encode_3d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer,
+              uint32_t box_blocks, bool bf16, uint64_t pitch_elems) {
+    if (inner % 64 != 0) return GEMM_ERR_INVALID_ARG;
+    cuuint64_t dims[3] = {64, outer, inner / 64};
+    cuuint64_t strides[2] = {(pitch_elems ? pitch_elems : inner) * 2, 128};
+    cuuint32_t box[3] = {64, box_outer, box_blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                          const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+}
+
 template <int kMode>
 int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, const CUtensorMap& ta,
                 const CUtensorMap& tb, const CUtensorMap& tb2, const CUtensorMap& tc, cudaStream_t st) {
@@ -233,9 +254,12 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     unsigned n_attr = 1;
-    if (pl.cluster > 1) {
+    // CTA pairs and cluster split-K: `cluster` CTAs per worker; A multicast:
+    // clusters of `mcast` one-CTA workers
+    const unsigned cdim = (unsigned)pl.cluster * (pl.mcast > 1 ? (unsigned)pl.mcast : 1u);
+    if (cdim > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)pl.cluster;
+        attr[1].val.clusterDim.x = cdim;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         n_attr = 2;
@@ -365,6 +389,11 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     const bool swap = (pl.path == 3);
     // the swapped kernel's exchange buffer holds one peer's partial
     if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
+    // A multicast pairs column-neighbour tiles of the 128 x 64 / 128 x 128 kernels
+    if (pl.mcast > 1 && (pl.mcast != 2 || pl.path != 2 || (pl.mma_n != 64 && pl.mma_n != 128) ||
+                         pl.block_k != 2 * kBlockK || pl.cluster != 1 || pl.tiles_n % 2 != 0 ||
+                         pl.grid % 2 != 0 || pl.dp_tiles != pl.num_tiles))
+        return GEMM_ERR_INVALID_ARG;
     int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16, a_pitch);
     if (rc != GEMM_OK) return rc;
     CUtensorMap tb2;
@@ -388,6 +417,35 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         tb2 = tb;
     }
     if (rc != GEMM_OK) return rc;
+    // One copy per operand and stage where the shapes allow (the TMA unit
+    // pays a fixed cost per copy, so fewer, larger boxes stream faster):
+    // A's 64-k blocks of a 128-k stage (K a multiple of 64), B's 64-column
+    // chunks when one CTA takes two or more whole chunks (N a multiple of 64),
+    // B stored (N, K) like A.  Off with the ":no3d" tuning suffix.
+    const bool no3d = force != nullptr && strstr(force, ":no3d") != nullptr;
+    const uint32_t sub = (uint32_t)pl.block_k / kBlockK;  // 64-k blocks per stage
+    if (!no3d && sub == 2 && K % 64 == 0 && pl.mcast <= 1) {
+        rc = encode_3d(&ta, A, (uint64_t)K, (uint64_t)M, swap ? (uint32_t)pl.tile_m : 128u, sub, bf16, a_pitch);
+        if (rc != GEMM_OK) return rc;
+        kp.a3d = 1;
+    }
+    if (!no3d && (!swap || pl.tile_n == 128)) {
+        if (b_nk) {
+            if (sub == 2 && K % 64 == 0) {
+                const uint32_t rows = swap ? 128u : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
+                rc = encode_3d(&tb, B, (uint64_t)K, (uint64_t)N, rows, sub, bf16, b_pitch);
+                if (rc != GEMM_OK) return rc;
+                kp.b3d = 1;
+            }
+        } else {
+            const uint32_t cols = swap ? 128u : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
+            if (N % 64 == 0 && cols % 64 == 0 && cols >= 128) {
+                rc = encode_3d(&tb, B, (uint64_t)N, (uint64_t)K, (uint32_t)pl.block_k, cols / 64, bf16, b_pitch);
+                if (rc != GEMM_OK) return rc;
+                kp.b3d = 1;
+            }
+        }
+    }
     // C: 64-column x 32-row boxes, one per epilogue warp and chunk
     CUtensorMap tc;
     rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32, bf16);

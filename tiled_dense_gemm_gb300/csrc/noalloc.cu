@@ -139,7 +139,7 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     gemm_relu_plan_t pl;
     rc = plan_problem(M, N, K, s.sm_count, -1, "swap", &pl);  // no clusters: plain launch
     if (rc != GEMM_OK) return rc;
-    if (pl.path != 3) return GEMM_ERR_TOO_LARGE;
+    if (pl.path != 3 || pl.cluster != 1 || pl.mcast != 1) return GEMM_ERR_TOO_LARGE;
     const size_t partial_bytes = (size_t)pl.workspace_bytes;
     if ((size_t)pl.counter_count * (1 + (size_t)pl.max_slots) > kMaxCounters ||
         partial_bytes > kScratchBytes - kPartialOffset)

@@ -158,6 +158,7 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
                        int32_t mma_n, int32_t narrow_n = 0) {
     p.path = path;
     p.mma_n = mma_n;
+    p.mcast = 1;
     p.cluster = (path == 4) ? 2 : 1;
     p.mma_m = (path == 4) ? 256 : 128;
     if (path == 2) {
@@ -305,6 +306,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         K > GEMM_RELU_MAX_DIM || num_sms < 1)
         return GEMM_ERR_INVALID_ARG;
     memset(plan, 0, sizeof(*plan));
+    plan->mcast = 1;
     if (M == 0 || N == 0) {
         plan->path = 0;
         return GEMM_OK;
@@ -467,6 +469,17 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // kernel streams B once: a copy would triple its traffic.)
     plan->pack = 0;
     if (contains(f, ":pk") && !contains(f, ":npk") && (plan->path == 2 || plan->path == 4)) plan->pack = 1;
+    // A multicast: two CTAs of a cluster take the two tiles of a column
+    // pair; each fetches one of the two 64-k boxes of every A stage and the
+    // TMA writes it into both (so each SM requests 3/4 (128 x 64 tiles) or
+    // 2/3 (128 x 128) of the bytes it consumes).  Data-parallel plans of
+    // the one-CTA kernel with 128-row stages and an even number of tile
+    // columns and of CTAs.
+    plan->mcast = 1;
+    if (contains(f, ":mc") && plan->path == 2 && (plan->mma_n == 64 || plan->mma_n == 128) &&
+        plan->block_k == 2 * kBlockK && plan->cluster == 1 && plan->splits <= 1 && plan->sk_tiles == 0 &&
+        plan->dp_tiles == plan->num_tiles && plan->tiles_n % 2 == 0 && plan->grid % 2 == 0 && pairs > 0)
+        plan->mcast = 2;
     return GEMM_OK;
 }
 

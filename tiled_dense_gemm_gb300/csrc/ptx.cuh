@@ -64,6 +64,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// tma_load_2d whose box is written, at the same shared-memory offset, into
+// every CTA of `cta_mask` in the cluster, each copy completing `bar` at that
+// offset in its own CTA.
+__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                  int32_t x, int32_t y, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
 // L2 policy that marks lines as the first to evict: for an operand that
 // every CTA together reads exactly once, so that it does not push reused
 // data out of L2.
@@ -99,6 +111,33 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int32_t x,
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(m)),
                  "r"(x), "r"(y)
+                 : "memory");
+}
+
+// 3-D tiled copies: a tensor map whose third dimension steps 128 bytes
+// along a row (64 two-byte elements) views a row-major matrix as 64-wide
+// column blocks; one copy of a box of several blocks lands them one after
+// another in shared memory (block-major, each 128B-swizzled like a 2-D box).
+__device__ __forceinline__ void tma_load_3d_maybe_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
+                                                       int32_t y, int32_t z, bool hinted, uint64_t policy) {
+    if (hinted)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+            " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+            : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* m, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
                  : "memory");
 }
 
@@ -253,6 +292,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// tma_load_3d for a CTA pair: completion on the leader's mbarrier.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x,
+                                                 int32_t y, int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // kCG selects the CTA group: 1 (one CTA) or 2 (a CTA pair sharing one MMA).
 // Every tcgen05 instruction of a kernel uses the same group.
@@ -329,6 +378,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t cta_mask = 1) 
             " [%0], %1;" ::"r"(bar),
             "h"(cta_mask)
             : "memory");
+}
+
+// One-CTA MMAs: arrive (once) on `bar` in every CTA of `cta_mask` when
+// every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
