@@ -1,10 +1,11 @@
 // Persistent, warp-specialised C = ReLU(A . B) kernel for sm_103a.
 //
-// Per CTA (192 threads, one CTA per SM; in the paired mode two CTAs on two
+// Per CTA (224 threads, one CTA per SM; in the paired mode two CTAs on two
 // SMs form a cluster and share each MMA, tcgen05 cta_group::2):
-//   warp 0      TMA producer: one thread streams A and B k-blocks into a
-//               ring of shared-memory stages (128-byte swizzle), each stage
-//               guarded by a full/empty mbarrier pair;
+//   warps 0, 6  TMA producers: one thread each streams A's (warp 0) and B's
+//               (warp 6) k-blocks into a ring of shared-memory stages
+//               (128-byte swizzle), each stage guarded by a full/empty
+//               mbarrier pair;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
 //               (fp16 or bf16 inputs -> fp32, 128 x N x 16 per instruction) into one
 //               of two TMEM accumulators and commits stage releases;
@@ -39,7 +40,7 @@
 
 namespace gr {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr uint32_t kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;  // named barrier id for the epilogue warps
 constexpr int kMaxStagesDev = 16;
@@ -195,6 +196,7 @@ struct Producer {
     WorkIter wi;
     WorkItem w;
     bool have_item;
+    bool armed;  // the current stage's empty wait and expect are done (prime)
     int32_t kb, a_row, b_col;
     uint32_t s, ph;
     // an operand that only one row (column) of tiles reads is streamed
@@ -206,12 +208,13 @@ struct Producer {
     uint32_t b_sub_bytes;  // swapped, B stored (N, K): bytes of one 64-k box of the tile's B rows
     bool mc;               // A multicast: this CTA fetches box `rank` of each A stage for both CTAs
     bool a3d, b3d;         // one 3-D copy per operand and stage (see KParams)
+    int32_t part;          // copies this thread issues: 0 all, 1 A's (and arms each stage), 2 B's
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
-                                        const CUtensorMap* tmB2_, int32_t worker, uint32_t rank_)
+                                        const CUtensorMap* tmB2_, int32_t worker, uint32_t rank_, int32_t part_ = 0)
         : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), tmB2(tmB2_), pl(p_.plan), stages(stages_), stride(stride_),
-          a_bytes(a_bytes_), rank(rank_), have_item(false), kb(0), a_row(0), b_col(0), s(0), ph(0) {
+          a_bytes(a_bytes_), rank(rank_), have_item(false), armed(false), kb(0), a_row(0), b_col(0), s(0), ph(0) {
         S = (uint32_t)pl.num_stages;
         full0 = smem_u32(&ctrl->full[0]);
         empty0 = smem_u32(&ctrl->empty[0]);
@@ -226,6 +229,7 @@ struct Producer {
         mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
         a3d = p_.a3d != 0;
         b3d = p_.b3d != 0;
+        part = part_;
         pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
     }
@@ -283,132 +287,168 @@ struct Producer {
             tma_load_2d_mcast(dst, m, bar, x, y, 0x3);
     }
 
+    // Move to the next work item; false when there is none.
+    __device__ __forceinline__ bool next_item() {
+        if (!wi.next(pl, w)) return false;
+        have_item = true;
+        kb = w.kb0;
+        // first row of A and first column of B this CTA loads
+        if constexpr (T::kPair) {
+            a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
+            b_col = w.tn * (int32_t)T::kBN + (int32_t)T::kBCols * (int32_t)rank;
+        } else if constexpr (!T::kSwap) {
+            a_row = w.tm * 128;
+            b_col = w.tn * (int32_t)T::kBN;
+        } else {
+            a_row = w.tm * pl.tile_m;
+            b_col = w.tn * pl.tile_n;
+        }
+        return true;
+    }
+
+    // Everything before the first copy, for a call ahead of the dependency
+    // wait so that it overlaps the previous kernel: the first work item
+    // (parameters and arithmetic) and the first stage's expected-bytes
+    // arrival (shared memory; the ring is fresh, so stage 0 needs no empty
+    // wait).
+    __device__ __forceinline__ void prime() {
+        if (!have_item && !next_item()) return;
+        if (s == 0 && ph == 0 && !armed) {
+            arm();
+            armed = true;
+        }
+    }
+
+    // Expect the stage's bytes on its full barrier (a pair: the leader's,
+    // which counts both CTAs' copies).
+    __device__ __forceinline__ void arm() {
+        if (part != 2 && (!T::kPair || rank == 0)) mbar_arrive_expect_tx(full0 + 8u * s, tx_bytes);
+    }
+
+    // The stage's copies from A's tensor map (its rows; the MMA B operand
+    // when swapped) ...
+    template <bool kPre>
+    __device__ __forceinline__ void copies_a(uint32_t full, uint32_t a_dst, uint32_t b_dst, int32_t k0) {
+        if constexpr (T::kPair) {
+            const uint32_t full_leader = mapa_shared(full, 0);
+            if (a3d) {
+                ld3_pair<kPre>(a_dst, tmA, full_leader, a_row, k0 / kBlockK);
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < T::kSub; ++i)
+                    ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
+            }
+        } else if constexpr (!T::kSwap) {
+            if (T::kSub == 2 && mc) {
+                // one of the stage's two A boxes; the peer fetches the other,
+                // and each lands in both CTAs
+                ld_mc<kPre>(a_dst + rank * kOperandA, tmA, full, k0 + (int32_t)(rank * kBlockK), a_row);
+            } else if (a3d) {
+                ld3<kPre>(a_dst, tmA, full, a_row, k0 / kBlockK, once_a);
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < T::kSub; ++i)
+                    ld<kPre>(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row, once_a);
+            }
+        } else {
+            // MMA B operand: the (padded) rows of A, one box per 64 k
+            if (a3d) {
+                ld3<kPre>(b_dst, tmA, full, a_row, k0 / kBlockK, once_a);
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
+                    ld<kPre>(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row, once_a);
+            }
+        }
+    }
+
+    // ... and from B's (the MMA A operand when swapped).
+    template <bool kPre>
+    __device__ __forceinline__ void copies_b(uint32_t full, uint32_t a_dst, uint32_t b_dst, int32_t k0) {
+        constexpr uint32_t kBChunk = T::kBK * kSwizzleRow;  // one 64-column chunk of B (K, N)
+        if constexpr (T::kPair) {
+            const uint32_t full_leader = mapa_shared(full, 0);
+            if (b_nk) {
+                // this CTA's kBCols rows of B, one K-major box per 64 k
+                if (b3d) {
+                    ld3_pair<kPre>(b_dst, tmB, full_leader, b_col, k0 / kBlockK);
+                } else {
+#pragma unroll
+                    for (uint32_t i = 0; i < T::kSub; ++i)
+                        ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
+                                      k0 + (int32_t)(i * kBlockK), b_col);
+                }
+            } else if (T::kBRem == 0 && b3d) {
+                // all of this CTA's 64-column chunks in one copy
+                ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
+            } else {
+                if constexpr (T::kBFull > 0) {
+#pragma unroll
+                    for (uint32_t j = 0; j < T::kBFull; ++j)
+                        ld_pair<kPre>(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
+                }
+                if constexpr (T::kBRem != 0)
+                    ld_pair<kPre>(b_dst + T::kBFull * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)T::kBFull,
+                                  k0);
+            }
+        } else if constexpr (!T::kSwap) {
+            if (b_nk && b3d) {
+                ld3<kPre>(b_dst, tmB, full, b_col, k0 / kBlockK, once_b);
+            } else if (b_nk) {
+                // the tile's kBN rows of B, K-major like A, one box per 64 k
+#pragma unroll
+                for (uint32_t i = 0; i < T::kSub; ++i)
+                    ld<kPre>(b_dst + i * T::kBN * kSwizzleRow, tmB, full, k0 + (int32_t)(i * kBlockK), b_col,
+                             once_b);
+            } else if (b3d) {
+                // all of the tile's 64-column chunks in one copy
+                ld3<kPre>(b_dst, tmB, full, k0, b_col / 64, once_b);
+            } else {
+#pragma unroll
+                for (uint32_t j = 0; j < T::kBN / 64; ++j)
+                    ld<kPre>(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0, once_b);
+            }
+        } else {
+            // MMA A operand: the tile's columns of B, one 64-wide chunk of kBK
+            // k-rows per TMA box (a narrow tile fills part of one chunk)
+            if (b3d) {
+                // one copy: the tile's B rows (B stored (N, K)) for every
+                // 64 k, or both 64-column chunks (B (K, N))
+                if (b_nk)
+                    ld3<kPre>(a_dst, tmB, full, b_col, k0 / kBlockK, once_b);
+                else
+                    ld3<kPre>(a_dst, tmB, full, k0, b_col / 64, once_b);
+            } else if (b_nk) {
+                // B stored (N, K): the tile's B rows, one K-major box per 64 k
+#pragma unroll
+                for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
+                    ld<kPre>(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK), b_col, once_b);
+            } else {
+                ld<kPre>(a_dst, tmB, full, b_col, k0, once_b);
+                if (pl.tile_n > 64) ld<kPre>(a_dst + kBChunk, tmB, full, b_col + 64, k0, once_b);
+            }
+        }
+    }
+
     template <bool kPre>
     __device__ __forceinline__ bool run(int32_t budget) {
         while (budget != 0) {
             if (!have_item || kb == w.kb1) {
-                if (!wi.next(pl, w)) return true;
-                have_item = true;
-                kb = w.kb0;
-                // first row of A and first column of B this CTA loads
-                if constexpr (T::kPair) {
-                    a_row = w.tm * (int32_t)T::kTileM + 128 * (int32_t)rank;
-                    b_col = w.tn * (int32_t)T::kBN + (int32_t)T::kBCols * (int32_t)rank;
-                } else if constexpr (!T::kSwap) {
-                    a_row = w.tm * 128;
-                    b_col = w.tn * (int32_t)T::kBN;
-                } else {
-                    a_row = w.tm * pl.tile_m;
-                    b_col = w.tn * pl.tile_n;
-                }
+                if (!next_item()) return true;
             }
-            if constexpr (!kPre)
-                if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return false;
+            if constexpr (!kPre) {
+                if (!armed) {
+                    if (!wait_phase(empty0 + 8u * s, ph ^ 1u, ctrl, p, kErrProducer)) return false;
+                    arm();
+                }
+                armed = false;
+            }
             const uint32_t full = full0 + 8u * s;
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
             const int32_t k0 = kb * (int32_t)T::kBK;
-            constexpr uint32_t kBChunk = T::kBK * kSwizzleRow;  // one 64-column chunk of B (K, N)
-            if constexpr (T::kPair) {
-                const uint32_t full_leader = mapa_shared(full, 0);
-                if (!kPre && rank == 0) mbar_arrive_expect_tx(full, tx_bytes);
-                if (a3d) {
-                    ld3_pair<kPre>(a_dst, tmA, full_leader, a_row, k0 / kBlockK);
-                } else {
-#pragma unroll
-                    for (uint32_t i = 0; i < T::kSub; ++i)
-                        ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
-                }
-                if (b_nk) {
-                    // this CTA's kBCols rows of B, one K-major box per 64 k
-                    if (b3d) {
-                        ld3_pair<kPre>(b_dst, tmB, full_leader, b_col, k0 / kBlockK);
-                    } else {
-#pragma unroll
-                        for (uint32_t i = 0; i < T::kSub; ++i)
-                            ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
-                                          k0 + (int32_t)(i * kBlockK), b_col);
-                    }
-                } else if (T::kBRem == 0 && b3d) {
-                    // all of this CTA's 64-column chunks in one copy
-                    ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
-                } else {
-                    if constexpr (T::kBFull > 0) {
-#pragma unroll
-                        for (uint32_t j = 0; j < T::kBFull; ++j)
-                            ld_pair<kPre>(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
-                    }
-                    if constexpr (T::kBRem != 0)
-                        ld_pair<kPre>(b_dst + T::kBFull * kBChunk, tmB2, full_leader,
-                                      b_col + 64 * (int32_t)T::kBFull, k0);
-                }
-            } else {
-                if constexpr (!kPre) mbar_arrive_expect_tx(full, tx_bytes);
-                if constexpr (!T::kSwap) {
-                    if (T::kSub == 2 && mc) {
-                        // one of the stage's two A boxes; the peer fetches the
-                        // other, and each lands in both CTAs
-                        ld_mc<kPre>(a_dst + rank * kOperandA, tmA, full, k0 + (int32_t)(rank * kBlockK), a_row);
-                    } else if (a3d) {
-                        ld3<kPre>(a_dst, tmA, full, a_row, k0 / kBlockK, once_a);
-                    } else {
-#pragma unroll
-                        for (uint32_t i = 0; i < T::kSub; ++i)
-                            ld<kPre>(a_dst + i * kOperandA, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                     once_a);
-                    }
-                    if (b_nk && b3d) {
-                        ld3<kPre>(b_dst, tmB, full, b_col, k0 / kBlockK, once_b);
-                    } else if (b_nk) {
-                        // the tile's kBN rows of B, K-major like A, one box per 64 k
-#pragma unroll
-                        for (uint32_t i = 0; i < T::kSub; ++i)
-                            ld<kPre>(b_dst + i * T::kBN * kSwizzleRow, tmB, full,
-                                     k0 + (int32_t)(i * kBlockK), b_col, once_b);
-                    } else if (b3d) {
-                        // all of the tile's 64-column chunks in one copy
-                        ld3<kPre>(b_dst, tmB, full, k0, b_col / 64, once_b);
-                    } else {
-#pragma unroll
-                        for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                            ld<kPre>(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0,
-                                     once_b);
-                    }
-                } else {
-                    // MMA A operand: the tile's columns of B, one 64-wide chunk
-                    // of kBK k-rows per TMA box (a narrow tile fills part of
-                    // one chunk)
-                    constexpr uint32_t kSwapChunk = T::kBK * kSwizzleRow;
-                    if (b3d) {
-                        // one copy: the tile's B rows (B stored (N, K)) for
-                        // every 64 k, or both 64-column chunks (B (K, N))
-                        if (b_nk)
-                            ld3<kPre>(a_dst, tmB, full, b_col, k0 / kBlockK, once_b);
-                        else
-                            ld3<kPre>(a_dst, tmB, full, k0, b_col / 64, once_b);
-                    } else if (b_nk) {
-                        // B stored (N, K): the tile's B rows, one K-major box
-                        // per 64 k
-#pragma unroll
-                        for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                            ld<kPre>(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK),
-                                     b_col, once_b);
-                    } else {
-                        ld<kPre>(a_dst, tmB, full, b_col, k0, once_b);
-                        if (pl.tile_n > 64)
-                            ld<kPre>(a_dst + kSwapChunk, tmB, full, b_col + 64, k0, once_b);
-                    }
-                    // MMA B operand: the (padded) rows of A, one box per 64 k
-                    if (a3d) {
-                        ld3<kPre>(b_dst, tmA, full, a_row, k0 / kBlockK, once_a);
-                    } else {
-#pragma unroll
-                        for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                            ld<kPre>(b_dst + i * a_sub_bytes, tmA, full, k0 + (int32_t)(i * kBlockK), a_row,
-                                     once_a);
-                    }
-                }
-            }
+            if (part != 2) copies_a<kPre>(full, a_dst, b_dst, k0);
+            if (part != 1) copies_b<kPre>(full, a_dst, b_dst, k0);
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -476,6 +516,12 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     wi.init(pl, worker, (int32_t)rank);
     WorkItem w;
     uint32_t s = 0, ph = 0, local = 0;
+    // The set-up above reads only parameters, so it overlaps the previous
+    // kernel (pinned here so that it is not sunk past the wait); the loop
+    // reads only shared and tensor memory, but its timeout path writes the
+    // error word, so it starts after the wait.
+    asm volatile("" : "+l"(a_desc0), "+l"(b_desc0)::"memory");
+    grid_dependency_wait();
     while (wi.next(pl, w)) {
         const uint32_t buf = local & 1u;
         const uint32_t bph = (local >> 1) & 1u;
@@ -1071,23 +1117,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // read or write global memory before that kernel has completed.  The
     // next kernel may start launching now: it waits the same way.
     grid_launch_dependents();
-    if (warp == 2 && lane == 0) {
-        // Warm L2 with the boxes of this CTA's first k-blocks (two rings'
-        // worth for the small-M kernel, which streams B from DRAM) while the
-        // previous kernel finishes: an idle epilogue warp issues the
-        // prefetches, so the producer is not held up (see Producer::prefetch).
-        Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
-        pre.prefetch((T::kSwap ? 2 : 1) * pl.num_stages);
-    }
-    grid_dependency_wait();
-
-    if (warp == 0) {
+    if (warp == 0 || warp == 6) {
         if (lane == 0) {
-            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
+            // Two producer threads, one per operand: a single thread issues
+            // one TMA copy per ~250-450 cycles, so two in parallel stream
+            // faster.  Warp 0 issues A's copies and arms each stage, warp 6
+            // B's.  The set-up (parameters, first work item) touches no
+            // global memory, so it runs before the wait too; only the copies
+            // come after it.
+            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank,
+                                 warp == 0 ? 1 : 2);
+            prod.prime();
+            grid_dependency_wait();
             prod.issue(-1);
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else {
+        if (T::kSwap && warp == 2 && lane == 0) {
+            // Small M: warm L2 with the boxes of this CTA's first two rings
+            // of k-blocks (B streams from DRAM) while the previous kernel
+            // finishes; an idle epilogue warp issues the prefetches (see
+            // Producer::prefetch).  (The tiled kernels measured faster
+            // without: their prefetches hold up the first copies in the TMA
+            // unit.)
+            Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
+            pre.prefetch(2 * pl.num_stages);
+        }
+        // (the MMA thread waits inside its role, after its set-up)
+        if (warp != 1) grid_dependency_wait();
+    }
+
+    if (warp == 1) {
         if (lane == 0 && (!T::kPair || rank == 0)) {  // one thread (of a pair's leader) issues the MMAs
             mma_role<kMode>(p, ctrl, stages, stride, a_bytes, tmem_base, worker, rank);
             // no MMA may still be running when tensor memory is released
@@ -1095,13 +1155,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_phase_for(smem_u32(&ctrl->final_bar), 0, p.timeout_ns)) atomicCAS(p.err, 0, kErrFinal);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // C staging for the TMA stores sits after the ring (tiled paths)
         const uint32_t staging = stages + (uint32_t)pl.num_stages * stride;
         epilogue_role<kMode>(p, ctrl, tmem_base, worker, rank, &tmC, stages, staging);
     }
 
-    if (warp == 0 && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
+    if ((warp == 0 || warp == 6) && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
         // aborting: give copies already issued time to land before the
         // shared memory is released
         const uint64_t t0 = globaltimer_ns();
