@@ -53,7 +53,9 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["stage_bytes"] == (128 + d["mma_n"] // 2) * d["block_k"] * 2
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
     assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
-    assert d["block_k"] == (64 if (d["path"] in (2, 4) and d["mma_n"] == 256) else 128)
+    want_bk = 64 if (d["path"] in (2, 4) and d["mma_n"] == 256) else 128
+    # (":bk128" gives 256-column CTA pairs 128-row stages)
+    assert d["block_k"] == want_bk or (forced and d["path"] == 4 and d["mma_n"] == 256 and d["block_k"] == 128)
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
     assert d["pack"] in (0, 1) and (d["pack"] == 0 or d["path"] in (2, 4))
@@ -141,7 +143,7 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
                                    "tiled128:sk", "pair128", "pair128:dp", "pair128:s3", "tiled64",
                                    "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2", "pair64",
                                    "pair64:s2", "tiled64:mc", "tiled128:mc", "tiled256:mc",
-                                   "tiled64:mc:s3", "tiled128:mc:c2"])
+                                   "tiled64:mc:s3", "tiled128:mc:c2", "pair:bk128", "pair:bk128:t2"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "pair128": (4, 128),

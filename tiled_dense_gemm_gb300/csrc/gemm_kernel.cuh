@@ -79,7 +79,10 @@ struct KParams {
     int32_t out_bf16;     // elements are bfloat16 (inputs and C) instead of binary16
     // 3-D tensor maps (64-element column blocks as a third dimension): one
     // copy fetches all 64-k blocks of a stage's A rows (a3d), or all
-    // 64-column chunks / 64-k blocks of its B (b3d), instead of one copy each
+    // 64-column chunks / 64-k blocks of its B (b3d), instead of one copy each.
+    // B stored (K, N) with N not a multiple of 64: the 3-D map covers the
+    // whole chunks only, and a CTA whose columns reach the partial chunk
+    // loads 64-column 2-D boxes through the second map of B instead.
     int32_t a3d, b3d;
     uint32_t idesc;
     uint64_t timeout_ns;
@@ -97,11 +100,12 @@ struct KParams {
 // 128 x 64; 6: CTA pair, C tile 256 x 192 (each CTA holds 96 columns of B:
 // one 64-wide chunk and a half-filled one, whose 32 columns come through a
 // second tensor map of B when B is stored (K, N)); 7: CTA pair, C tile
-// 256 x 64 (each CTA holds 32 columns of B, a half-filled chunk).
+// 256 x 64 (each CTA holds 32 columns of B, a half-filled chunk); 8: as 3,
+// with ring stages of 128 k-rows (8 MMAs per stage instead of 4).
 template <int kMode>
 struct ModeTraits {
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6 || kMode == 7);
+    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6 || kMode == 7 || kMode == 8);
     static constexpr int kCG = kPair ? 2 : 1;
     static constexpr uint32_t kBN = (kMode == 5 || kMode == 7)   ? 64
                                     : (kMode == 1 || kMode == 4) ? 128
@@ -208,6 +212,7 @@ struct Producer {
     uint32_t b_sub_bytes;  // swapped, B stored (N, K): bytes of one 64-k box of the tile's B rows
     bool mc;               // A multicast: this CTA fetches box `rank` of each A stage for both CTAs
     bool a3d, b3d;         // one 3-D copy per operand and stage (see KParams)
+    bool b_edge;           // B (K, N), b3d: this item's columns reach past the 3-D map's whole chunks
     int32_t part;          // copies this thread issues: 0 all, 1 A's (and arms each stage), 2 B's
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
@@ -229,6 +234,7 @@ struct Producer {
         mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
         a3d = p_.a3d != 0;
         b3d = p_.b3d != 0;
+        b_edge = false;
         part = part_;
         pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
@@ -302,6 +308,10 @@ struct Producer {
         } else {
             a_row = w.tm * pl.tile_m;
             b_col = w.tn * pl.tile_n;
+        }
+        {
+            constexpr int32_t kChunks = T::kSwap ? 2 : (int32_t)(T::kPair ? T::kBCols : T::kBN) / 64;
+            b_edge = b_col / 64 + kChunks > (int32_t)(p.N / 64);
         }
         return true;
     }
@@ -378,9 +388,14 @@ struct Producer {
                         ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
                                       k0 + (int32_t)(i * kBlockK), b_col);
                 }
-            } else if (T::kBRem == 0 && b3d) {
+            } else if (T::kBRem == 0 && b3d && !b_edge) {
                 // all of this CTA's 64-column chunks in one copy
                 ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
+            } else if (T::kBRem == 0 && b3d) {
+                // the partial last chunk: 2-D boxes through the second map
+#pragma unroll
+                for (uint32_t j = 0; j < T::kBFull; ++j)
+                    ld_pair<kPre>(b_dst + j * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)j, k0);
             } else {
                 if constexpr (T::kBFull > 0) {
 #pragma unroll
@@ -400,24 +415,30 @@ struct Producer {
                 for (uint32_t i = 0; i < T::kSub; ++i)
                     ld<kPre>(b_dst + i * T::kBN * kSwizzleRow, tmB, full, k0 + (int32_t)(i * kBlockK), b_col,
                              once_b);
-            } else if (b3d) {
+            } else if (b3d && !b_edge) {
                 // all of the tile's 64-column chunks in one copy
                 ld3<kPre>(b_dst, tmB, full, k0, b_col / 64, once_b);
             } else {
+                // (b3d: the partial last chunk, through the 2-D second map)
+                const CUtensorMap* m2 = b3d ? tmB2 : tmB;
 #pragma unroll
                 for (uint32_t j = 0; j < T::kBN / 64; ++j)
-                    ld<kPre>(b_dst + j * kBChunk, tmB, full, b_col + 64 * (int32_t)j, k0, once_b);
+                    ld<kPre>(b_dst + j * kBChunk, m2, full, b_col + 64 * (int32_t)j, k0, once_b);
             }
         } else {
             // MMA A operand: the tile's columns of B, one 64-wide chunk of kBK
             // k-rows per TMA box (a narrow tile fills part of one chunk)
-            if (b3d) {
+            if (b3d && (b_nk || !b_edge)) {
                 // one copy: the tile's B rows (B stored (N, K)) for every
                 // 64 k, or both 64-column chunks (B (K, N))
                 if (b_nk)
                     ld3<kPre>(a_dst, tmB, full, b_col, k0 / kBlockK, once_b);
                 else
                     ld3<kPre>(a_dst, tmB, full, k0, b_col / 64, once_b);
+            } else if (b3d) {
+                // the partial last chunk: 2-D boxes through the second map
+                ld<kPre>(a_dst, tmB2, full, b_col, k0, once_b);
+                ld<kPre>(a_dst + kBChunk, tmB2, full, b_col + 64, k0, once_b);
             } else if (b_nk) {
                 // B stored (N, K): the tile's B rows, one K-major box per 64 k
 #pragma unroll

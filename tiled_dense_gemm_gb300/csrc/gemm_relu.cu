@@ -67,7 +67,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[8] = {false, false, false, false, false, false, false, false};
+    bool attr_set[9] = {false, false, false, false, false, false, false, false, false};
     std::vector<StreamBuffers> streams;
 };
 
@@ -438,9 +438,12 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
                 kp.b3d = 1;
             }
         } else {
+            // (N not a multiple of 64: the map covers the whole chunks; a CTA
+            // reaching the partial one uses the 2-D map, kept in tb2)
             const uint32_t cols = swap ? 128u : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-            if (N % 64 == 0 && cols % 64 == 0 && cols >= 128) {
-                rc = encode_3d(&tb, B, (uint64_t)N, (uint64_t)K, (uint32_t)pl.block_k, cols / 64, bf16, b_pitch);
+            if (N >= 64 && cols % 64 == 0 && cols >= 128) {
+                rc = encode_3d(&tb, B, (uint64_t)(N / 64) * 64, (uint64_t)K, (uint32_t)pl.block_k, cols / 64, bf16,
+                               b_pitch ? b_pitch : (uint64_t)N);
                 if (rc != GEMM_OK) return rc;
                 kp.b3d = 1;
             }
@@ -462,6 +465,7 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         if (pl.mma_n == 128) return launch_mode<4>(d, pl, kp, ta, tb, tb2, tc, st);
         if (pl.mma_n == 192) return launch_mode<6>(d, pl, kp, ta, tb, tb2, tc, st);
         if (pl.mma_n == 64) return launch_mode<7>(d, pl, kp, ta, tb, tb2, tc, st);
+        if (pl.block_k == 2 * kBlockK) return launch_mode<8>(d, pl, kp, ta, tb, tb2, tc, st);
         return launch_mode<3>(d, pl, kp, ta, tb, tb2, tc, st);
     }
     if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tb2, tc, st);

@@ -155,7 +155,7 @@ static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t 
 // Fill the shape-dependent fields for one kernel shape.  `narrow_n` (path 3
 // only) is a C tile width of at most 64 columns, else 0 for 128.
 static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path,
-                       int32_t mma_n, int32_t narrow_n = 0) {
+                       int32_t mma_n, int32_t narrow_n = 0, bool long_stages = false) {
     p.path = path;
     p.mma_n = mma_n;
     p.mcast = 1;
@@ -176,7 +176,9 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
     p.num_tiles = p.tiles_m * p.tiles_n;
     // k-rows per stage: 128, except 256-column tiles (tensor-bound already;
     // 64-row stages keep their ring deeper)
-    p.block_k = (mma_n == 256 && path != 3) ? kBlockK : 2 * kBlockK;
+    // (CTA pairs with 256-column tiles take 128-row stages when asked:
+    // ":bk128")
+    p.block_k = (mma_n == 256 && path != 3 && !(long_stages && path == 4)) ? kBlockK : 2 * kBlockK;
     p.num_kb = (int32_t)((K + p.block_k - 1) / p.block_k);
     p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
     // per CTA: columns of the MMA B operand it loads (half of the tile for
@@ -324,6 +326,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     const bool dp_only = contains(f, ":dp");
     const bool force_csk = contains(f, ":c2");
     const bool force_sk = contains(f, ":sk");
+    const bool long_stages = contains(f, ":bk128");
     int32_t force_tail = 0;  // ":tS": full waves data-parallel, leftover tiles split S ways
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 't' && q[2] >= '0' && q[2] <= '9') force_tail = q[2] - '0';
@@ -376,7 +379,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     auto take = [&](int32_t path, int32_t mma_n, int32_t workers) {
         gemm_relu_plan_t q;
         memset(&q, 0, sizeof(q));
-        shape_plan(q, M, N, K, path, mma_n);
+        shape_plan(q, M, N, K, path, mma_n, 0, long_stages);
         double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2, pairs);
         if (force_tail > 1 && q.num_tiles >= workers && q.num_tiles % workers != 0) {
             q.cluster = (path == 4) ? 2 : 1;
