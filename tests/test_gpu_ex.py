@@ -75,7 +75,7 @@ SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (48, 61
 FORCES = ["", "tiled256", "tiled128", "pair", "tiled256:dp", "swap", "swap:dp", "swapn56", "swapn8",
           "swap:c2", "tiled128:c2", "swap:s7", "tiled128:s3", "pair:s5", "swap:sk", "pair128",
           "pair128:s3", "tiled64", "tiled64:c2", "pair192", "pair192:s2", "pair64",
-          "pair:pk", "tiled128:pk", "tiled64:mc", "tiled128:mc", "tiled128:no3d", "pair:no3d", "swap:no3d", "pair:bk128"]
+          "pair:pk", "tiled128:pk", "tiled64:mc", "tiled128:mc", "tiled128:no3d", "pair:no3d", "swap:no3d", "pair:bk128", "tiled256:c2"]
 
 
 @pytest.mark.parametrize("force", FORCES)

@@ -64,6 +64,7 @@ struct __align__(8) Ctrl {
     uint64_t tmem_empty[2];
     uint64_t final_bar;
     uint64_t exch_bar;  // cluster split-K: the peers' partials are ready (rank 0)
+    uint64_t peer_free;  // tiled cluster split-K: the peer's ring is idle (its MMAs are done)
     uint64_t fix_bar[4];  // split-K fixup of a CTA's final item: 64-column units of the partials landed
     uint32_t tmem_addr;
     int32_t abort_flag;
@@ -393,9 +394,11 @@ struct Producer {
                 ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
             } else if (T::kBRem == 0 && b3d) {
                 // the partial last chunk: 2-D boxes through the second map
+                if constexpr (T::kBFull > 0) {
 #pragma unroll
-                for (uint32_t j = 0; j < T::kBFull; ++j)
-                    ld_pair<kPre>(b_dst + j * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)j, k0);
+                    for (uint32_t j = 0; j < T::kBFull; ++j)
+                        ld_pair<kPre>(b_dst + j * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)j, k0);
+                }
             } else {
                 if constexpr (T::kBFull > 0) {
 #pragma unroll
@@ -739,12 +742,81 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
             //     ring; the plan reserves one slot, cluster = 2) with
             //     asynchronous remote stores whose bytes complete rank 0's
             //     exchange barrier; rank 0 reads them locally.
-            //   tiled: rank r > 0 leaves its partial in its own ring and
-            //     arrives on rank 0's barrier; rank 0 reads it over DSMEM.
+            //   tiled, >= 128 columns: a symmetric exchange (below);
+            //   tiled, narrower: rank r > 0 leaves its partial in its own
+            //     ring and arrives on rank 0's barrier; rank 0 reads it over
+            //     DSMEM.
             // The cluster barrier at teardown keeps the ranks alive until
             // rank 0 is done.
             const uint32_t exch = smem_u32(&ctrl->exch_bar);
             const uint32_t slot_bytes = ncols * 128u * 4u;
+            // bounded wait, with cluster acquire, on a one-shot barrier
+            auto wait_cluster = [&](uint32_t bar) {
+                const uint64_t t0 = globaltimer_ns();
+                volatile int32_t* abort_flag = &ctrl->abort_flag;
+                while (!mbar_try_wait_acq_cluster(bar, 0)) {
+                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                        *abort_flag = 1;
+                        atomicCAS(p.err, 0, kErrEpilogue);
+                        return false;
+                    }
+                }
+                return true;
+            };
+            if (!T::kSwap && pl.cluster == 2 && ncols >= 128) {
+                // Tiled, two ranks: a symmetric exchange.  Rank r owns the
+                // columns [r * h, (r + 1) * h) of the tile (h = ncols / 2).
+                // Once both rings are idle (each rank's MMAs are done), each
+                // rank pushes the other's columns of its fp32 accumulator
+                // into the other's ring (asynchronous remote stores whose
+                // bytes complete the receiver's exchange barrier), then sums
+                // its own columns -- rank 0's K range first -- and stores them.
+                const uint32_t h = ncols / 2;
+                const uint32_t peer = rank ^ 1u;
+                if (threadIdx.x == 64) mbar_arrive_cluster(mapa_shared(smem_u32(&ctrl->peer_free), peer));
+                bool ready = named_bar_and(kEpiBarrier, kEpiThreads, wait_cluster(smem_u32(&ctrl->peer_free)));
+                if (!ready) {
+                    release_tmem();
+                    break;
+                }
+                const uint32_t xbuf = mapa_shared(stages, peer);
+                const uint32_t xbar = mapa_shared(exch, peer);
+                for (uint32_t c = 0; c < h; c += kChunk) {
+                    __syncwarp();
+                    tmem_load_chunk<kMode>(taddr + peer * h + c, v);
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j)
+                        st_async_v4_cluster(xbuf + (((c / 4 + j) * 128u + lane_row) << 4),
+                                            make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]),
+                                                       __float_as_uint(v[4 * j + 2]), __float_as_uint(v[4 * j + 3])),
+                                            xbar);
+                }
+                ready = named_bar_and(kEpiBarrier, kEpiThreads, wait_cluster(exch));
+                if (!ready) {
+                    release_tmem();
+                    break;
+                }
+                for (uint32_t c = 0; c < h; c += kChunk) {
+                    __syncwarp();
+                    tmem_load_chunk<kMode>(taddr + rank * h + c, v);
+                    float4 x[kQ];
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) x[j] = ld_shared_f4(stages + (((c / 4 + j) * 128u + lane_row) << 4));
+                    // (rank 0's share + rank 1's: fp32 addition of two terms
+                    // does not depend on the operand order)
+#pragma unroll
+                    for (int j = 0; j < kQ; ++j) {
+                        v[4 * j] += x[j].x;
+                        v[4 * j + 1] += x[j].y;
+                        v[4 * j + 2] += x[j].z;
+                        v[4 * j + 3] += x[j].w;
+                    }
+                    sink(w, rank * h + c);
+                }
+                release_tmem();
+                ++local;
+                continue;
+            }
             if (T::kSwap && rank != 0) {
                 const uint32_t xbuf = mapa_shared(staging + (rank - 1u) * slot_bytes, 0);
                 const uint32_t xbar = mapa_shared(exch, 0);
@@ -779,20 +851,7 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
                 ++local;
                 continue;
             }
-            bool ready = true;
-            {
-                const uint64_t t0 = globaltimer_ns();
-                volatile int32_t* abort_flag = &ctrl->abort_flag;
-                while (!mbar_try_wait_acq_cluster(exch, 0)) {
-                    if (*abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
-                        *abort_flag = 1;
-                        atomicCAS(p.err, 0, kErrEpilogue);
-                        ready = false;
-                        break;
-                    }
-                }
-            }
-            ready = named_bar_and(kEpiBarrier, kEpiThreads, ready);
+            bool ready = named_bar_and(kEpiBarrier, kEpiThreads, wait_cluster(exch));
             if (!ready) {
                 release_tmem();
                 break;
@@ -1113,7 +1172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // cluster split-K: swapped, the peers push their partials into this
         // CTA's buffer (one local arrival, completed by their bytes); tiled,
         // each peer arrives once its partial sits in its own ring
-        mbar_init(smem_u32(&ctrl->exch_bar), (!T::kSwap && pl.cluster > 1) ? (uint32_t)pl.cluster - 1u : 1u);
+        // (tiled, cluster of 2 and >= 128 columns: the symmetric exchange --
+        // one local arrival, completed by the peer's pushed bytes)
+        const bool sym_exch = !T::kSwap && cluster_split(pl) && pl.cluster == 2 && pl.mma_n >= 128;
+        mbar_init(smem_u32(&ctrl->exch_bar),
+                  (!T::kSwap && pl.cluster > 1 && !sym_exch) ? (uint32_t)pl.cluster - 1u : 1u);
+        mbar_init(smem_u32(&ctrl->peer_free), 1);
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
         fence_mbar_init();
@@ -1121,6 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (T::kSwap && cluster_split(pl) && rank == 0)
             mbar_arrive_expect_tx(smem_u32(&ctrl->exch_bar),
                                   ((uint32_t)pl.cluster - 1u) * (uint32_t)pl.mma_n * 128u * 4u);
+        if (sym_exch) mbar_arrive_expect_tx(smem_u32(&ctrl->exch_bar), (uint32_t)pl.mma_n / 2u * 128u * 4u);
     }
     if (warp == 1) {
         tmem_alloc<T::kCG>(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
