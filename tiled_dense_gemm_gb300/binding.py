@@ -207,10 +207,14 @@ def gemm_relu_host(a, b, c=None, apply_relu: bool = True, stream=None, device=No
     N = b.shape[1]
     if c is None:
         c = torch.empty((M, N), dtype=torch.float16, pin_memory=a.is_pinned())
-    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    with torch.cuda.device(dev):
-        rc = lib().gemm_relu_host(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
-                                  int(bool(apply_relu)), _stream_handle(stream, dev))
+    cur = torch.cuda.current_device()
+    dev = torch.device("cuda", cur) if device is None else torch.device(device)
+    args = (a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K, int(bool(apply_relu)), _stream_handle(stream, dev))
+    if dev.index is None or dev.index == cur:
+        rc = lib().gemm_relu_host(*args)
+    else:
+        with torch.cuda.device(dev):
+            rc = lib().gemm_relu_host(*args)
     if rc != GEMM_OK:
         raise GemmReluError(rc, "gemm_relu_host")
     return c

@@ -59,6 +59,7 @@ struct StreamBuffers {
     void* hB = nullptr;
     void* hC = nullptr;
     size_t hA_bytes = 0, hB_bytes = 0, hC_bytes = 0;
+    int32_t* h_err = nullptr;  // pinned copy of the error word (host-buffer entry point)
 };
 
 struct DeviceState {
@@ -473,6 +474,18 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     return launch_mode<1>(d, pl, kp, ta, tb, tb2, tc, st);
 }
 
+// A launch gave up part-way (the error word is set): clear it and every
+// counter, and report the timeout.  Caller holds g_mu.
+int reset_after_error_locked(DeviceState& d) {
+    cudaDeviceSynchronize();
+    cudaMemset(d.d_err, 0, 16);
+    for (auto& s : d.streams)
+        if (s.counters) cudaMemset(s.counters, 0, s.counter_bytes);
+    cudaDeviceSynchronize();
+    cudaGetLastError();
+    return GEMM_ERR_TIMEOUT;
+}
+
 }  // namespace
 }  // namespace gr
 
@@ -506,6 +519,7 @@ extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_ho
     int dev;
     if ((rc = current_device(&dev)) != GEMM_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t* h_err = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if ((rc = init_device_locked(dev)) != GEMM_OK) return rc;
@@ -524,13 +538,30 @@ extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_ho
         if (rc == GEMM_OK &&
             cudaMemcpyAsync(C_host, sb.hC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
             rc = GEMM_ERR_CUDA;
+        // the error word comes back in the same stream, so one synchronize
+        // covers the copies, the kernel and the check
+        if (rc == GEMM_OK && !sb.h_err && cudaHostAlloc(&sb.h_err, sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
+            sb.h_err = nullptr;
+            rc = GEMM_ERR_OUT_OF_MEMORY;
+        }
+        if (rc == GEMM_OK &&
+            cudaMemcpyAsync(sb.h_err, d.d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            rc = GEMM_ERR_CUDA;
         if (rc != GEMM_OK) {
             cudaGetLastError();
             return rc;
         }
+        h_err = sb.h_err;
     }
-    return gemm_relu_check_device_error(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (*(volatile int32_t*)h_err == 0) return GEMM_OK;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return reset_after_error_locked(g_dev[dev]);
 }
+
 
 extern "C" int gemm_relu_check_device_error(void* stream) {
     int dev;
@@ -550,14 +581,7 @@ extern "C" int gemm_relu_check_device_error(void* stream) {
         return GEMM_ERR_CUDA;
     }
     if (err == 0) return GEMM_OK;
-    // a launch gave up part-way: clear the error word and every counter
-    cudaDeviceSynchronize();
-    cudaMemset(d.d_err, 0, 16);
-    for (auto& s : d.streams)
-        if (s.counters) cudaMemset(s.counters, 0, s.counter_bytes);
-    cudaDeviceSynchronize();
-    cudaGetLastError();
-    return GEMM_ERR_TIMEOUT;
+    return reset_after_error_locked(d);
 }
 
 extern "C" const char* gemm_relu_status_string(int status) {
@@ -593,6 +617,7 @@ extern "C" void gemm_relu_shutdown(void) {
                 cudaFree(s.hA);
                 cudaFree(s.hB);
                 cudaFree(s.hC);
+                if (s.h_err) cudaFreeHost(s.h_err);
             }
             cudaFree(d.d_err);
         }
