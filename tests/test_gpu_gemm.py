@@ -285,7 +285,7 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
                                    "pair64", "pair64:s2", "tiled128:pk", "pair:pk",
                                    "tiled64:pk", "pair:t2:pk", "tiled128:no3d", "pair:no3d",
                                    "swap:no3d", "tiled256:no3d", "pair128:no3d", "pair:bk128",
-                                   "pair:bk128:s3", "pair:bk128:no3d"])
+                                   "pair:bk128:s3", "pair:bk128:no3d", "pair:skt", "tiled128:skt"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel variant (one-CTA 128x256 / 128x128 tiles, CTA pairs,
     swapped operands with 128-wide or narrow tiles), with and without

@@ -143,7 +143,8 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
                                    "tiled128:sk", "pair128", "pair128:dp", "pair128:s3", "tiled64",
                                    "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2", "pair64",
                                    "pair64:s2", "tiled64:mc", "tiled128:mc", "tiled256:mc",
-                                   "tiled64:mc:s3", "tiled128:mc:c2", "pair:bk128", "pair:bk128:t2"])
+                                   "tiled64:mc:s3", "tiled128:mc:c2", "pair:bk128", "pair:bk128:t2",
+                                   "pair:skt", "tiled256:skt"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "pair128": (4, 128),
@@ -170,7 +171,7 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert d["dp_tiles"] == 0 and d["sk_tiles"] == d["num_tiles"] and d["splits"] == 1
             workers = 76 if d["path"] == 4 else 152  # CTA pairs on 152 SMs
             assert d["grid"] == min(workers, d["num_tiles"] * d["num_kb"])
-        elif ":s" in force:
+        elif ":s" in force and force.split(":s")[1][:1].isdigit():
             want_s = min(int(force.split(":s")[1]), d["num_kb"])
             assert d["dp_tiles"] == 0 and d["max_slots"] == want_s
             assert d["splits"] == (want_s if want_s > 1 else 1)

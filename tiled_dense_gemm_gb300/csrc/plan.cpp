@@ -325,8 +325,10 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     const char* f = force ? force : "";
     const bool dp_only = contains(f, ":dp");
     const bool force_csk = contains(f, ":c2");
-    const bool force_sk = contains(f, ":sk");
+    const bool force_sk = contains(f, ":sk") && !contains(f, ":skt");
     const bool long_stages = contains(f, ":bk128");
+    // ":skt": full waves but the last data-parallel, the rest stream-K
+    const bool force_sk_tail = contains(f, ":skt");
     int32_t force_tail = 0;  // ":tS": full waves data-parallel, leftover tiles split S ways
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 't' && q[2] >= '0' && q[2] <= '9') force_tail = q[2] - '0';
@@ -385,6 +387,12 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
             q.cluster = (path == 4) ? 2 : 1;
             const int32_t sp = force_tail < q.num_kb ? force_tail : q.num_kb;
             finish_split(q, workers, (q.num_tiles / workers) * workers, q.num_tiles % workers, sp);
+            cost = 0.0;
+        }
+        if (force_sk_tail && q.num_tiles > workers && q.num_tiles % workers != 0) {
+            q.cluster = (path == 4) ? 2 : 1;
+            const int32_t full = q.num_tiles / workers;
+            finish_split(q, workers, (full - 1) * workers, q.num_tiles - (full - 1) * workers);
             cost = 0.0;
         }
         if (force_sk) {
