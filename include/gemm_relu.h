@@ -216,8 +216,14 @@ typedef struct {
  * split every tile's K range between the two CTAs of a cluster, which
  * combine their halves through distributed shared memory ("pair" has no
  * ":c2": its cluster already holds one 256-row tile), or by ":sk" to run
- * every tile stream-K over all workers; ":pk" / ":npk" force / forbid the
- * packing of misaligned operands.
+ * every tile stream-K over all workers, or by ":tS" for full data-parallel
+ * waves with the leftover tiles cut into S K ranges, or by ":skt" for the
+ * full waves but the last data-parallel and the rest stream-K; ":pk" /
+ * ":npk" force / forbid the packing of misaligned operands; ":mc" runs the
+ * 128 x 64 / 128 x 128 kernels in clusters of two column-neighbour tiles that
+ * share each A stage by TMA multicast (data-parallel plans only); ":bk128"
+ * gives 256 x 256 CTA pairs ring stages of 128 k-rows; ":no3d" keeps every
+ * TMA copy two-dimensional (one copy per 64-k block or 64-column chunk).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);
