@@ -45,11 +45,26 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
 
 # ----------------------------------------------------------------- helpers
 
-def kernel_source_hash() -> str:
+def code_without_comments(text: str) -> str:
+    """C/C++ source with comments, blank lines and trailing blanks removed
+    (string literals in these sources hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash(read=None) -> str:
+    """Hash of the kernel and launch sources, comments aside: traffic taken
+    with ncu stays valid while only comments change."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "tiled_dense_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, "tiled_dense_gemm_gb300", "csrc", f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(code_without_comments(text).encode())
     return h.hexdigest()[:16]
 
 

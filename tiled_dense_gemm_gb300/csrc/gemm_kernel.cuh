@@ -185,8 +185,9 @@ __device__ __forceinline__ uint16_t round16(float x, int32_t bf16) {
 // adding to their start-address field (a 14-bit field of 16-byte units that
 // cannot carry: shared addresses stay below 256 KiB).
 
-// The TMA producer: one thread walks the work items and k-blocks, waits for
-// a free ring stage, and issues the stage's copies.  issue() keeps its
+// A TMA producer thread walks the work items and k-blocks, waits for a free
+// ring stage, and issues the stage's copies (the kernel runs two: one for
+// A's copies, which also arms each stage, one for B's).  issue() keeps its
 // position between calls.
 template <int kMode>
 struct Producer {
@@ -195,13 +196,15 @@ struct Producer {
     Ctrl* ctrl;
     const CUtensorMap* tmA;
     const CUtensorMap* tmB;
-    const CUtensorMap* tmB2;  // (K, N) storage: boxes of the last partial chunk (pair, 256 x 192)
+    // second map of B (K, N): boxes of a pair CTA's last partial chunk
+    // (256 x 192), or 64-column 2-D boxes when tmB is a 3-D map
+    const CUtensorMap* tmB2;
     gemm_relu_plan_t pl;
     uint32_t stages, stride, a_bytes, rank, S, full0, empty0, tx_bytes;
     WorkIter wi;
     WorkItem w;
     bool have_item;
-    bool armed;  // the current stage's empty wait and expect are done (prime)
+    bool armed;  // the current stage's expected bytes are armed already (prime: stage 0 of the fresh ring)
     int32_t kb, a_row, b_col;
     uint32_t s, ph;
     // an operand that only one row (column) of tiles reads is streamed
