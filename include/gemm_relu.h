@@ -229,6 +229,30 @@ typedef struct {
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);
 
 /*
+ * The TMA boxes of the copies the kernel issues for one ring stage under
+ * *plan (host-only; used by the CPU tests, and by the library itself to
+ * encode its tensor maps).  Elements are 16-bit.  An operand whose stage is
+ * one 3-D copy views its row-major matrix as 64-element column blocks (a
+ * third dimension 128 bytes apart); a box of several blocks lands them block
+ * after block in shared memory.  b_layout is GEMM_B_KN or GEMM_B_NK; the
+ * ":no3d" suffix of GEMM_RELU_FORCE_PATH keeps every copy 2-D.
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for a null pointer or a plan
+ * without a kernel (path < 2).
+ */
+typedef struct {
+    int32_t a_3d;           /* 1: A's stage is one 3-D copy of a_box[2] 64-k blocks */
+    uint32_t a_box[3];      /* 64 (k), rows of A (128, or the padded M when swapped), 64-k blocks */
+    int32_t b_3d;           /* 1: B's stage is one 3-D copy */
+    uint32_t b_box[3];      /* B (K, N): columns (64, or a narrow swapped tile's width), k-rows, 64-column
+                               chunks; B (N, K): 64 (k), rows of N, 64-k blocks */
+    uint32_t b2_box[2];     /* B's second (2-D) map: columns (or 64 k), k-rows (or rows of N) */
+    int64_t b_view_inner;   /* 3-D B (K, N): the columns its view covers (whole 64-column chunks) */
+} gemm_relu_boxes_t;
+
+int gemm_relu_plan_boxes(const gemm_relu_plan_t* plan, int64_t M, int64_t N, int64_t K, int b_layout,
+                         gemm_relu_boxes_t* boxes);
+
+/*
  * The idx-th work item of worker `cta` under *plan, exactly as the kernel walks
  * it: C tile `tile` (tile_m_idx, tile_n_idx after rasterisation), k-blocks
  * [kb_begin, kb_end), and for a tile split along K its share `slot` of

@@ -228,3 +228,68 @@ def test_headline_shapes_use_the_intended_kernels(gemm_lib):
     # 64 tiles of 128 columns, each by a 2-CTA cluster (one K half each)
     assert sk.path == 3 and sk.mma_n == 16 and sk.tile_n == 128
     assert sk.cluster == 2 and sk.grid == 64 and sk.dp_tiles == 64
+
+
+def _check_boxes(gemm_lib, M, N, K, layout, no3d=False):
+    """The TMA boxes of one ring stage agree with the stage the kernel
+    reserves: the copies of a stage deliver exactly stage_bytes per CTA, a
+    3-D copy fills the shared-memory region of its operand, and no 3-D view
+    reaches past the end of a matrix row."""
+    p = gemm_lib.plan(M, N, K, 152)
+    d = p.as_dict()
+    if d["path"] < 2:
+        return
+    bx = gemm_lib.plan_boxes(p, M, N, K, layout).as_dict()
+    swap, pair = d["path"] == 3, d["path"] == 4
+    bk = d["block_k"]
+    sub = bk // 64
+    for box in (bx["a_box"], bx["b_box"]):
+        assert all(1 <= v <= 256 for v in box)
+    # A
+    rows_a = d["tile_m"] if swap else 128
+    assert bx["a_box"][:2] == [64, rows_a]
+    if bx["a_3d"]:
+        assert not no3d and K % 64 == 0 and sub == 2 and d["mcast"] == 1 and bx["a_box"][2] == sub
+    else:
+        assert bx["a_box"][2] == 1
+        assert no3d or K % 64 != 0 or sub == 1 or d["mcast"] == 2
+    a_bytes = 64 * rows_a * sub * 2  # one stage of A, 3-D or one 2-D box per 64-k block
+    # B
+    if layout == "kn":
+        cols = 128 if swap and d["tile_n"] > 64 else (d["tile_n"] if swap else (d["mma_n"] // 2 if pair else d["mma_n"]))
+        if bx["b_3d"]:
+            assert not no3d and N >= 64 and cols % 64 == 0 and cols >= 128
+            assert bx["b_box"] == [64, bk, cols // 64]
+            assert bx["b_view_inner"] == (N // 64) * 64 <= N
+            assert bx["b2_box"] == [64, bk]  # the partial chunk's 2-D boxes
+        else:
+            assert bx["b_box"][1] == bk and bx["b_box"][2] == 1
+            assert bx["b_box"][0] == (d["tile_n"] if swap and d["tile_n"] <= 64 else 64)
+            assert no3d or N < 64 or cols % 64 != 0 or cols < 128
+        b_bytes = cols * bk * 2
+    else:
+        rows_b = (d["tile_n"] if d["tile_n"] <= 64 else 128) if swap else (d["mma_n"] // 2 if pair else d["mma_n"])
+        assert bx["b_box"][:2] == [64, rows_b] and bx["b2_box"] == [64, rows_b]
+        if bx["b_3d"]:
+            assert not no3d and K % 64 == 0 and sub == 2 and (not swap or d["tile_n"] == 128)
+            assert bx["b_box"][2] == sub
+        else:
+            assert bx["b_box"][2] == 1
+        b_bytes = rows_b * 64 * sub * 2
+    assert a_bytes + b_bytes == d["stage_bytes"], (M, N, K, layout, d, bx)
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("force", ["", "tiled256", "tiled128", "tiled64", "pair", "pair128", "pair192", "pair64",
+                                   "swap", "swapn56", "swapn8", "pair:bk128", "tiled128:c2", "swap:c2",
+                                   "tiled64:mc", "tiled128:no3d", "pair:no3d", "swap:no3d"])
+def test_copy_boxes_match_the_stage(gemm_lib, monkeypatch, layout, force):
+    if force:
+        monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
+    else:
+        monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
+    rng = random.Random(3)
+    shapes = list(SHAPES) + [(rng.randint(1, 3000), 8 * rng.randint(1, 700), 8 * rng.randint(1, 600))
+                             for _ in range(25)]
+    for M, N, K in shapes:
+        _check_boxes(gemm_lib, M, N, K, layout, no3d=":no3d" in force)

@@ -44,6 +44,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+class Boxes(ctypes.Structure):
+    """gemm_relu_boxes_t: the TMA boxes of one ring stage's copies."""
+    _fields_ = [("a_3d", ctypes.c_int32), ("a_box", ctypes.c_uint32 * 3), ("b_3d", ctypes.c_int32),
+                ("b_box", ctypes.c_uint32 * 3), ("b2_box", ctypes.c_uint32 * 2), ("b_view_inner", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {"a_3d": self.a_3d, "a_box": list(self.a_box), "b_3d": self.b_3d, "b_box": list(self.b_box),
+                "b2_box": list(self.b2_box), "b_view_inner": self.b_view_inner}
+
+
 def declared_functions() -> list[str]:
     """Names of the functions include/gemm_relu.h declares."""
     text = open(os.path.join(INCLUDE, "gemm_relu.h")).read()
@@ -80,6 +90,8 @@ def lib():
         L.gemm_relu_plan.restype = i32
         L.gemm_relu_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(Plan)]
         p32 = ctypes.POINTER(ctypes.c_int32)
+        L.gemm_relu_plan_boxes.restype = i32
+        L.gemm_relu_plan_boxes.argtypes = [ctypes.POINTER(Plan), i64, i64, i64, i32, ctypes.POINTER(Boxes)]
         L.gemm_relu_plan_work_item.restype = i32
         L.gemm_relu_plan_work_item.argtypes = [ctypes.POINTER(Plan), i32, i32] + [p32] * 7
         _lib = L
@@ -113,6 +125,15 @@ def plan_work_items(p: Plan, cta: int) -> list[dict]:
         out.append(dict(zip(("tile", "tm", "tn", "kb0", "kb1", "slot", "nslots"),
                             (v.value for v in vals))))
         idx += 1
+
+
+def plan_boxes(p: Plan, M: int, N: int, K: int, b_layout: str = "kn") -> Boxes:
+    """The TMA boxes the kernel's copies use for one ring stage under plan ``p``."""
+    out = Boxes()
+    rc = lib().gemm_relu_plan_boxes(ctypes.byref(p), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(out))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu_plan_boxes")
+    return out
 
 
 def _stream_handle(stream, device):

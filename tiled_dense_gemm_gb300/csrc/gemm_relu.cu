@@ -395,61 +395,39 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
                          pl.block_k != 2 * kBlockK || pl.cluster != 1 || pl.tiles_n % 2 != 0 ||
                          pl.grid % 2 != 0 || pl.dp_tiles != pl.num_tiles))
         return GEMM_ERR_INVALID_ARG;
-    int rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, swap ? (uint32_t)pl.tile_m : 128u, bf16, a_pitch);
+    // the boxes of one stage's copies (3-D where the shapes allow)
+    gemm_relu_boxes_t bx;
+    int rc = plan_boxes(pl, M, N, K, b_nk, force, &bx);
     if (rc != GEMM_OK) return rc;
+    if (bx.a_3d)
+        rc = encode_3d(&ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[1], bx.a_box[2], bf16, a_pitch);
+    else
+        rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[0], bx.a_box[1], bf16, a_pitch);
+    if (rc != GEMM_OK) return rc;
+    kp.a3d = bx.a_3d;
     CUtensorMap tb2;
     if (!b_nk) {
-        // B (K, N): 64-column boxes of one stage's block_k k-rows (a narrow
-        // swapped tile: one box of tile_n columns)
-        rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K,
-                       (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u, (uint32_t)pl.block_k, bf16, b_pitch);
-        // a pair CTA whose B columns end in a partial chunk (256 x 192
-        // tiles: 96 columns) loads that chunk with narrower boxes
-        const uint32_t rem = (pl.path == 4) ? (uint32_t)(pl.mma_n / 2) % 64u : 0u;
-        if (rc == GEMM_OK && rem)
-            rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, rem, (uint32_t)pl.block_k, bf16, b_pitch);
-        else
-            tb2 = tb;
-    } else {
-        // B (N, K): boxes of 64 k by the rows of N one CTA loads per stage
-        const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
-                                   : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-        rc = encode_2d(&tb, B, (uint64_t)K, (uint64_t)N, kBlockK, rows, bf16, b_pitch);
-        tb2 = tb;
-    }
-    if (rc != GEMM_OK) return rc;
-    // One copy per operand and stage where the shapes allow (the TMA unit
-    // pays a fixed cost per copy, so fewer, larger boxes stream faster):
-    // A's 64-k blocks of a 128-k stage (K a multiple of 64), B's 64-column
-    // chunks when one CTA takes two or more whole chunks (N a multiple of 64),
-    // B stored (N, K) like A.  Off with the ":no3d" tuning suffix.
-    const bool no3d = force != nullptr && strstr(force, ":no3d") != nullptr;
-    const uint32_t sub = (uint32_t)pl.block_k / kBlockK;  // 64-k blocks per stage
-    if (!no3d && sub == 2 && K % 64 == 0 && pl.mcast <= 1) {
-        rc = encode_3d(&ta, A, (uint64_t)K, (uint64_t)M, swap ? (uint32_t)pl.tile_m : 128u, sub, bf16, a_pitch);
-        if (rc != GEMM_OK) return rc;
-        kp.a3d = 1;
-    }
-    if (!no3d && (!swap || pl.tile_n == 128)) {
-        if (b_nk) {
-            if (sub == 2 && K % 64 == 0) {
-                const uint32_t rows = swap ? 128u : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-                rc = encode_3d(&tb, B, (uint64_t)K, (uint64_t)N, rows, sub, bf16, b_pitch);
-                if (rc != GEMM_OK) return rc;
-                kp.b3d = 1;
-            }
-        } else {
-            // (N not a multiple of 64: the map covers the whole chunks; a CTA
-            // reaching the partial one uses the 2-D map, kept in tb2)
-            const uint32_t cols = swap ? 128u : (pl.path == 4 ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-            if (N >= 64 && cols % 64 == 0 && cols >= 128) {
-                rc = encode_3d(&tb, B, (uint64_t)(N / 64) * 64, (uint64_t)K, (uint32_t)pl.block_k, cols / 64, bf16,
+        // the second map: 2-D boxes (a pair CTA's partial chunk, or the
+        // partial chunk a 3-D view leaves out)
+        rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, bx.b2_box[0], bx.b2_box[1], bf16, b_pitch);
+        if (rc == GEMM_OK) {
+            if (bx.b_3d)
+                rc = encode_3d(&tb, B, (uint64_t)bx.b_view_inner, (uint64_t)K, bx.b_box[1], bx.b_box[2], bf16,
                                b_pitch ? b_pitch : (uint64_t)N);
-                if (rc != GEMM_OK) return rc;
-                kp.b3d = 1;
-            }
+            else
+                rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K, bx.b_box[0], bx.b_box[1], bf16, b_pitch);
+        }
+    } else {
+        rc = encode_2d(&tb2, B, (uint64_t)K, (uint64_t)N, bx.b2_box[0], bx.b2_box[1], bf16, b_pitch);
+        if (rc == GEMM_OK) {
+            if (bx.b_3d)
+                rc = encode_3d(&tb, B, (uint64_t)K, (uint64_t)N, bx.b_box[1], bx.b_box[2], bf16, b_pitch);
+            else
+                tb = tb2;
         }
     }
+    if (rc != GEMM_OK) return rc;
+    kp.b3d = bx.b_3d;
     // C: 64-column x 32-row boxes, one per epilogue warp and chunk
     CUtensorMap tc;
     rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32, bf16);

@@ -496,6 +496,76 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
 
 }  // namespace gr
 
+namespace gr {
+
+int plan_boxes(const gemm_relu_plan_t& pl, int64_t M, int64_t N, int64_t K, bool b_nk, const char* force,
+               gemm_relu_boxes_t* o) {
+    (void)M;
+    if (!o || pl.path < 2) return GEMM_ERR_INVALID_ARG;
+    memset(o, 0, sizeof(*o));
+    const bool swap = pl.path == 3;
+    const bool pair = pl.path == 4;
+    const uint32_t sub = (uint32_t)pl.block_k / kBlockK;  // 64-k blocks per stage
+    const uint32_t bk = (uint32_t)pl.block_k;
+    // One copy per operand and stage where the shapes allow (the TMA unit
+    // pays a fixed cost per copy, so fewer, larger boxes stream faster).
+    const bool allow3d = !(force && strstr(force, ":no3d"));
+    // A: 64 k by 128 rows (the padded rows of A when swapped) per 64-k
+    // block; one 3-D copy of a stage's two blocks when K is a multiple of 64
+    // (the 2-D A boxes of the multicast kernel stay)
+    o->a_box[0] = kBlockK;
+    o->a_box[1] = swap ? (uint32_t)pl.tile_m : 128u;
+    o->a_box[2] = 1;
+    if (allow3d && sub == 2 && K % kBlockK == 0 && pl.mcast <= 1) {
+        o->a_3d = 1;
+        o->a_box[2] = sub;
+    }
+    if (!b_nk) {
+        // B (K, N): 64-column boxes of a stage's k-rows (a narrow swapped
+        // tile: one box of its width); a pair CTA whose columns end in a
+        // partial chunk (256 x 192: 96 columns) loads it through the second
+        // map with narrower boxes
+        o->b_box[0] = (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u;
+        o->b_box[1] = bk;
+        o->b_box[2] = 1;
+        const uint32_t rem = pair ? (uint32_t)(pl.mma_n / 2) % 64u : 0u;
+        o->b2_box[0] = rem ? rem : o->b_box[0];
+        o->b2_box[1] = bk;
+        // all of a CTA's whole chunks in one 3-D copy (two or more); with N
+        // not a multiple of 64 the view covers the whole chunks, and a CTA
+        // reaching the partial one uses the second (2-D) map
+        const uint32_t cols = swap ? 128u : (pair ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
+        if (allow3d && (!swap || pl.tile_n == 128) && N >= 64 && cols % 64 == 0 && cols >= 128) {
+            o->b_3d = 1;
+            o->b_box[0] = 64;
+            o->b_box[2] = cols / 64;
+            o->b_view_inner = (N / 64) * 64;
+        }
+    } else {
+        // B (N, K): 64 k by the rows of N one CTA loads per stage
+        const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
+                                   : (pair ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
+        o->b_box[0] = kBlockK;
+        o->b_box[1] = rows;
+        o->b_box[2] = 1;
+        o->b2_box[0] = kBlockK;
+        o->b2_box[1] = rows;
+        if (allow3d && (!swap || pl.tile_n == 128) && sub == 2 && K % kBlockK == 0) {
+            o->b_3d = 1;
+            o->b_box[2] = sub;
+        }
+    }
+    return GEMM_OK;
+}
+
+}  // namespace gr
+
+extern "C" int gemm_relu_plan_boxes(const gemm_relu_plan_t* plan, int64_t M, int64_t N, int64_t K, int b_layout,
+                                    gemm_relu_boxes_t* boxes) {
+    if (!plan || (b_layout != GEMM_B_KN && b_layout != GEMM_B_NK)) return GEMM_ERR_INVALID_ARG;
+    return gr::plan_boxes(*plan, M, N, K, b_layout == GEMM_B_NK, getenv("GEMM_RELU_FORCE_PATH"), boxes);
+}
+
 extern "C" int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms,
                               gemm_relu_plan_t* plan) {
     return gr::plan_problem(M, N, K, num_sms, 0, getenv("GEMM_RELU_FORCE_PATH"), plan);

@@ -180,4 +180,9 @@ struct WorkIter {
 int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, const char* force,
                  gemm_relu_plan_t* plan);
 
+// The TMA boxes of one ring stage's copies under `plan` (3-D where the
+// shapes allow, unless `force` holds ":no3d").  Defined in plan.cpp.
+int plan_boxes(const gemm_relu_plan_t& plan, int64_t M, int64_t N, int64_t K, bool b_nk, const char* force,
+               gemm_relu_boxes_t* boxes);
+
 }  // namespace gr
