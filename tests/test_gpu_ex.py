@@ -71,7 +71,7 @@ def inputs_and_ref(shape, layout, dtype, relu, seed=31):
 
 
 SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (48, 6144, 2048),
-          (8, 4864, 1024)]
+          (8, 4864, 1024), (16, 1000, 1024)]
 FORCES = ["", "tiled256", "tiled128", "pair", "tiled256:dp", "swap", "swap:dp", "swapn56", "swapn8",
           "swap:c2", "tiled128:c2", "swap:s7", "tiled128:s3", "pair:s5", "swap:sk", "pair128",
           "pair128:s3", "tiled64", "tiled64:c2", "pair192", "pair192:s2", "pair64",

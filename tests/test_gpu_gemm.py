@@ -273,7 +273,8 @@ def test_stream_k_counters_are_left_zero():
 # ---------------------------------------------------------------- every kernel shape
 
 FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (1024, 1024, 1024),
-                 (257, 1032, 4104), (96, 2048, 3000), (48, 6144, 2048), (8, 4864, 1024)]
+                 (257, 1032, 4104), (96, 2048, 3000), (48, 6144, 2048), (8, 4864, 1024),
+                 (16, 1000, 1024), (100, 1000, 1032)]
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "tiled128:dp",
