@@ -112,6 +112,18 @@ int gemm_relu_host(const void* A_host, const void* B_host, void* C_host,
  * word.  Returns GEMM_ERR_TIMEOUT if a kernel of this library gave up a
  * bounded wait since the last check (the split-K counters are then reset),
  * GEMM_ERR_CUDA if the stream reports a CUDA error, else GEMM_OK.
+ *
+ * Every device wait of the kernels is bounded (2 s plus 2 us per k-block);
+ * a CTA whose wait runs out records the error, stops its other roles, lets
+ * its copies and MMAs in flight land, frees its tensor memory and returns.
+ * Test hook of that path (tests only): with the environment variable
+ * GEMM_RELU_TEST_DROP_KB=k set, gemm_relu, gemm_relu_ex and
+ * gemm_relu_noalloc launch with every CTA leaving the copies of k-block k
+ * of its first work item undone and with every wait limited to 1 ms, so
+ * that the wait for that k-block runs out and the launch ends with the
+ * error recorded (its C is incomplete).  A k outside [0, number of
+ * k-blocks of the plan) or a plan that runs in clusters is refused with
+ * GEMM_ERR_INVALID_ARG.
  */
 int gemm_relu_check_device_error(void* stream);
 
@@ -151,17 +163,34 @@ void gemm_relu_shutdown(void);
  *
  * The first call on a device does a one-time set-up there (device check,
  * the scratch array's device address via cudaGetSymbolAddress, kernel
- * attributes); make that first call before any stream capture.  Every call
- * on a device shares the one array and finds it as the previous call left
- * it: each call first clears, on `stream`, the counters and error word it
- * needs to start at zero.  Calls whose execution overlaps on the GPU (e.g.
- * on two streams) race on the array and give undefined results; issue them
- * in one stream or otherwise ordered.  A timed-out device wait in this
- * variant is recorded in the array's error word, not in the word that
- * gemm_relu_check_device_error reads.
+ * attributes); make that first call before any stream capture.  With CUDA's
+ * default lazy module loading, that first call is also when the driver
+ * loads this code's module on the device, which reserves the array and the
+ * kernel image (about GEMM_RELU_NOALLOC_SCRATCH_BYTES plus a few hundred
+ * KiB of device memory): a caller that later reserves all remaining device
+ * memory should make the first call at initialisation, before doing so.
+ * Every call on a device shares the one array and finds it as the previous
+ * call left it: each call first clears, on `stream`, the split-K counters
+ * it needs to start at zero.  Calls whose execution overlaps on the GPU
+ * (e.g. on two streams) race on the array and give undefined results;
+ * issue them in one stream or otherwise ordered.  A timed-out device wait
+ * in this variant is recorded in the array's own error word, which stays
+ * set until gemm_relu_noalloc_check_device_error reads and clears it.
  */
 int gemm_relu_noalloc(const void* A, const void* B, void* C,
                       int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);
+
+/*
+ * The error check of gemm_relu_noalloc, which allocates nothing either:
+ * synchronizes `stream`, reads the fixed array's error word on the current
+ * device with one 4-byte copy, and clears the word (and the split-K
+ * counters) if it was set.  Returns GEMM_ERR_TIMEOUT if a gemm_relu_noalloc
+ * kernel on this device gave up a bounded wait since the last check (the C
+ * of that call is incomplete), GEMM_ERR_CUDA if the stream reports a CUDA
+ * error, GEMM_ERR_UNSUPPORTED_DEVICE if the device is not a GB300, else
+ * GEMM_OK.  Like gemm_relu_noalloc, it has no counterpart on the pages.
+ */
+int gemm_relu_noalloc_check_device_error(void* stream);
 
 /* ---- Host-only planning interface (no CUDA calls; usable without a GPU) -- */
 
@@ -189,13 +218,6 @@ typedef struct {
     int32_t stage_bytes; /* bytes of A and B tile per ring stage */
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
-    int32_t pack;        /* 1: before the GEMM, copy each operand whose row pitch is not a
-                            multiple of 128 bytes to a 128-byte pitch (library workspace);
-                            only when forced (":pk"), as it measured slower */
-    int32_t mcast;       /* 1, or 2: path 2 with 128 x 64 or 128 x 128 tiles, data-parallel only,
-                            launched in clusters of 2 CTAs that take the two column-neighbour
-                            tiles of one tile row; each CTA loads half of every A stage and
-                            the TMA multicasts it into both CTAs */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
     int64_t counter_count;   /* arrival counters (one per split tile and CTA of a worker); the
                                 counter array also holds max_slots ready flags per counter */
@@ -207,23 +229,17 @@ typedef struct {
  * num_sms / 2; the runtime also caps them by the device's co-resident
  * cluster count).  Pure host code.  The environment variable
  * GEMM_RELU_FORCE_PATH (tuning and tests only) restricts the choice:
- * "tiled256", "tiled128", "tiled64" (128 x 64 tiles), "swap" (M <= 128 only), "swapnW" (M <= 128,
- * data-parallel tiles W = 8..64 columns wide), "pair" (CTA pairs, 256 x
- * 256 tiles), "pair192", "pair128" or "pair64" (CTA pairs, 256 x 192 /
- * 256 x 128 / 256 x 64 tiles), optionally
- * followed by ":dp" to forbid splitting tiles along K, by ":sN" to cut
- * every tile into N equal K ranges (the split schedule), or by ":c2" to
- * split every tile's K range between the two CTAs of a cluster, which
- * combine their halves through distributed shared memory ("pair" has no
- * ":c2": its cluster already holds one 256-row tile), or by ":sk" to run
- * every tile stream-K over all workers, or by ":tS" for full data-parallel
- * waves with the leftover tiles cut into S K ranges, or by ":skt" for the
- * full waves but the last data-parallel and the rest stream-K; ":pk" /
- * ":npk" force / forbid the packing of misaligned operands; ":mc" runs the
- * 128 x 64 / 128 x 128 kernels in clusters of two column-neighbour tiles that
- * share each A stage by TMA multicast (data-parallel plans only); ":bk128"
- * gives 256 x 256 CTA pairs ring stages of 128 k-rows; ":no3d" keeps every
- * TMA copy two-dimensional (one copy per 64-k block or 64-column chunk).
+ * "tiled256", "tiled128", "tiled64" (128 x 256 / 128 x 128 / 128 x 64
+ * tiles, one CTA each), "pair" (CTA pairs, 256 x 256 tiles), "swap"
+ * (swapped operands, M <= 128 only), optionally followed by ":dp" to forbid
+ * splitting tiles along K, by ":sN" to cut every tile into N equal K ranges
+ * (the split schedule), by ":c2" to split every tile's K range between the
+ * two CTAs of a cluster, which combine their halves through distributed
+ * shared memory ("pair" has no ":c2": its cluster already holds one
+ * 256-row tile), by ":sk" to run every tile stream-K over all workers, or
+ * by ":tS" for full data-parallel waves with the leftover tiles cut into S
+ * K ranges; ":no3d" keeps every TMA copy two-dimensional (one copy per
+ * 64-k block or 64-column chunk).
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);
@@ -243,9 +259,9 @@ typedef struct {
     int32_t a_3d;           /* 1: A's stage is one 3-D copy of a_box[2] 64-k blocks */
     uint32_t a_box[3];      /* 64 (k), rows of A (128, or the padded M when swapped), 64-k blocks */
     int32_t b_3d;           /* 1: B's stage is one 3-D copy */
-    uint32_t b_box[3];      /* B (K, N): columns (64, or a narrow swapped tile's width), k-rows, 64-column
-                               chunks; B (N, K): 64 (k), rows of N, 64-k blocks */
-    uint32_t b2_box[2];     /* B's second (2-D) map: columns (or 64 k), k-rows (or rows of N) */
+    uint32_t b_box[3];      /* B (K, N): 64 columns, k-rows, 64-column chunks; B (N, K): 64 (k),
+                               rows of N, 64-k blocks */
+    uint32_t b2_box[2];     /* B's second (2-D) map: 64 columns (or 64 k), k-rows (or rows of N) */
     int64_t b_view_inner;   /* 3-D B (K, N): the columns its view covers (whole 64-column chunks) */
 } gemm_relu_boxes_t;
 

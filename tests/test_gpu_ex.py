@@ -72,10 +72,9 @@ def inputs_and_ref(shape, layout, dtype, relu, seed=31):
 
 SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (48, 6144, 2048),
           (8, 4864, 1024), (16, 1000, 1024)]
-FORCES = ["", "tiled256", "tiled128", "pair", "tiled256:dp", "swap", "swap:dp", "swapn56", "swapn8",
-          "swap:c2", "tiled128:c2", "swap:s7", "tiled128:s3", "pair:s5", "swap:sk", "pair128",
-          "pair128:s3", "tiled64", "tiled64:c2", "pair192", "pair192:s2", "pair64",
-          "pair:pk", "tiled128:pk", "tiled64:mc", "tiled128:mc", "tiled128:no3d", "pair:no3d", "swap:no3d", "pair:bk128", "tiled256:c2"]
+FORCES = ["", "tiled256", "tiled128", "pair", "tiled256:dp", "swap", "swap:dp", "swap:c2", "tiled128:c2",
+          "swap:s7", "tiled128:s3", "pair:s5", "swap:sk", "tiled64", "tiled64:c2", "tiled128:no3d", "pair:no3d",
+          "swap:no3d", "tiled256:c2", "pair:t2"]
 
 
 @pytest.mark.parametrize("force", FORCES)
@@ -108,25 +107,19 @@ def test_ex_skinny_full_parity(layout, dtype):
     assert_relu_sign(c, True, "c4_skinny")
 
 
+@pytest.mark.parametrize("name", ["c3_4096", "c5_ragged"])
 @pytest.mark.parametrize("layout,dtype", VARIANTS)
-def test_ex_square_4096_sampled_parity(layout, dtype):
-    """4096^3: whole tile rows / columns at both ends and in the middle,
-    plus random entries, each computed by the oracle in k order."""
-    w = WORKLOADS["c3_4096"]
+def test_ex_workload_full_parity(layout, dtype, name):
+    """4096^3 and the ragged workload (ReLU on and off) in each B layout /
+    element type: every output element against the oracle."""
+    w = WORKLOADS[name]
     A, B = make_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.scale_a, w.dist_b, w.scale_b,
                        dtype=TORCH_DTYPE[dtype], b_layout=layout)
-    c = gpu_ex(A, B, layout).double().numpy()
-    rng = np.random.default_rng(7)
-    rows = np.concatenate([np.arange(0, 3), np.arange(2046, 2050), np.arange(4093, 4096),
-                           rng.integers(0, 4096, 8)])
-    cols = np.concatenate([np.arange(0, 3), np.arange(2046, 2050), np.arange(4093, 4096),
-                           rng.integers(0, 4096, 8)])
-    rr, cc = np.meshgrid(rows, cols, indexing="ij")
-    ref = oracle.gemm_relu_entries_ex(A, B, rr.ravel(), cc.ravel(), True, layout, dtype,
-                                      threads=THREADS)
-    got = c[rr.ravel(), cc.ravel()]
-    ok = oracle.within_tolerance(got, ref)
-    assert ok.all(), f"{int((~ok).sum())} of {ok.size} sampled entries outside tolerance"
+    for relu in w.relu_modes:
+        ref = oracle.gemm_relu_ex(A, B, relu, layout, dtype, threads=THREADS)
+        c = gpu_ex(A, B, layout, relu)
+        assert_close(c, ref, f"{name} {layout}/{dtype} relu={relu}")
+        assert_relu_sign(c, relu, name)
 
 
 @pytest.mark.parametrize("layout,dtype", VARIANTS)

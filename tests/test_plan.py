@@ -42,28 +42,21 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
         assert d["sk_tiles"] == 0 and d["workspace_bytes"] == 0
     if d["path"] == 3:
         assert d["mma_n"] == ((M + 15) // 16) * 16
-        assert d["tile_n"] == 128 or (8 <= d["tile_n"] <= 64 and d["tile_n"] % 8 == 0 and d["sk_tiles"] == 0)
+        assert d["tile_n"] == 128
         assert d["mma_m"] == 128 and (d["cluster"] == 1 or csk)
     elif d["path"] == 2:
         assert d["mma_n"] in (64, 128, 256) and d["tile_m"] == 128
         assert d["mma_m"] == 128 and (d["cluster"] == 1 or csk)
     else:
-        assert d["mma_n"] in (64, 128, 192, 256)
+        assert d["mma_n"] == 256
         assert (d["mma_m"], d["tile_m"], d["tile_n"], d["cluster"]) == (256, 256, d["mma_n"], 2)
         assert d["stage_bytes"] == (128 + d["mma_n"] // 2) * d["block_k"] * 2
     assert d["mma_n"] % 16 == 0 and 16 <= d["mma_n"] <= 256
     assert d["tiles_m"] * d["tile_m"] >= M and d["tiles_n"] * d["tile_n"] >= N
     want_bk = 64 if (d["path"] in (2, 4) and d["mma_n"] == 256) else 128
-    # (":bk128" gives 256-column CTA pairs 128-row stages)
-    assert d["block_k"] == want_bk or (forced and d["path"] == 4 and d["mma_n"] == 256 and d["block_k"] == 128)
+    assert d["block_k"] == want_bk
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
-    assert d["pack"] in (0, 1) and (d["pack"] == 0 or d["path"] in (2, 4))
-    assert d["mcast"] in (1, 2)
-    if d["mcast"] == 2:
-        assert d["path"] == 2 and d["mma_n"] in (64, 128) and d["block_k"] == 128 and d["cluster"] == 1
-        assert d["tiles_n"] % 2 == 0 and d["grid"] % 2 == 0
-        assert d["dp_tiles"] == d["num_tiles"] and d["sk_tiles"] == 0 and d["splits"] <= 1
     assert d["smem_bytes"] <= SMEM_LIMIT
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
     assert 1 <= d["grid"] * d["cluster"] <= sms
@@ -101,14 +94,6 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
                 slots[it["tile"]][it["slot"]] = (it["kb0"], it["kb1"], it["nslots"])
         if d["sk_tiles"]:
             sk_units.append(units)
-        if d["mcast"] == 2 and cta % 2 == 1:
-            # the two CTAs of an A-multicast cluster walk the same tile rows
-            # and K ranges in lockstep, on the two tiles of a column pair
-            prev = gemm_lib.plan_work_items(p, cta - 1)
-            assert len(prev) == len(items)
-            for a, b in zip(prev, items):
-                assert a["tm"] == b["tm"] and (a["kb0"], a["kb1"]) == (b["kb0"], b["kb1"])
-                assert a["tn"] % 2 == 0 and b["tn"] == a["tn"] + 1
     # every unit exactly once
     assert len(cover) == d["num_tiles"] * d["num_kb"]
     assert set(cover.values()) == {1}
@@ -138,17 +123,12 @@ def test_schedule_covers_every_unit_once(gemm_lib, shape, sms):
 
 
 @pytest.mark.parametrize("force", ["tiled256", "tiled128", "pair", "tiled256:dp", "pair:dp",
-                                   "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3", "swapn56",
-                                   "swapn8", "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk",
-                                   "tiled128:sk", "pair128", "pair128:dp", "pair128:s3", "tiled64",
-                                   "tiled64:s3", "tiled64:c2", "pair192", "pair192:s2", "pair64",
-                                   "pair64:s2", "tiled64:mc", "tiled128:mc", "tiled256:mc",
-                                   "tiled64:mc:s3", "tiled128:mc:c2", "pair:bk128", "pair:bk128:t2",
-                                   "pair:skt", "tiled256:skt"])
+                                   "swap", "swap:dp", "swap:s19", "tiled128:s8", "pair:s3",
+                                   "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk",
+                                   "tiled128:sk", "tiled64", "tiled64:s3", "tiled64:c2", "pair:t2"])
 def test_forced_paths(gemm_lib, monkeypatch, force):
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
-    want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "pair128": (4, 128),
-            "tiled64": (2, 64), "pair192": (4, 192), "pair64": (4, 64)}
+    want = {"tiled256": (2, 256), "tiled128": (2, 128), "pair": (4, 256), "tiled64": (2, 64)}
     for shape in SHAPES:
         d = _check(gemm_lib, *shape, 152, forced=True)
         if force.startswith("swap"):
@@ -157,14 +137,6 @@ def test_forced_paths(gemm_lib, monkeypatch, force):
             assert (d["path"], d["mma_n"]) == want[force.split(":")[0]]
         if force.endswith(":dp"):
             assert d["sk_tiles"] == 0
-        if ":mc" not in force:
-            assert d["mcast"] == 1
-        elif force in ("tiled64:mc", "tiled128:mc"):
-            # every data-parallel plan with an even number of tile columns
-            assert d["mcast"] == (2 if d["tiles_n"] % 2 == 0 and d["dp_tiles"] == d["num_tiles"]
-                                  and d["grid"] % 2 == 0 and d["cluster"] == 1 else 1)
-        else:
-            assert d["mcast"] == 1 or (d["sk_tiles"] == 0 and d["cluster"] == 1)
         if ":c2" in force and d["num_tiles"] <= 76 and d["num_kb"] >= 2:
             assert d["cluster"] == 2 and d["grid"] == d["num_tiles"]
         if force.endswith(":sk"):
@@ -187,19 +159,6 @@ def test_tail_wave_split(gemm_lib, monkeypatch, force, sp):
         if T % workers:
             assert d["dp_tiles"] == (T // workers) * workers
             assert d["sk_tiles"] == T % workers and d["splits"] == sp and d["max_slots"] == sp
-
-
-def test_packing_decision(gemm_lib, monkeypatch):
-    monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
-    # only when forced (measured no faster on the ragged workload)
-    assert gemm_lib.plan(3000, 5000, 2056, 152).pack == 0
-    assert gemm_lib.plan(4096, 4096, 4096, 152).pack == 0
-    assert gemm_lib.plan(300, 264, 2056, 152).pack == 0
-    assert gemm_lib.plan(16, 8192, 8200, 152).pack == 0
-    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "tiled128:pk")
-    assert gemm_lib.plan(300, 264, 2056, 152).pack == 1
-    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "pair:npk")
-    assert gemm_lib.plan(3000, 5000, 2056, 152).pack == 0
 
 
 def test_random_shapes(gemm_lib):
@@ -249,14 +208,14 @@ def _check_boxes(gemm_lib, M, N, K, layout, no3d=False):
     rows_a = d["tile_m"] if swap else 128
     assert bx["a_box"][:2] == [64, rows_a]
     if bx["a_3d"]:
-        assert not no3d and K % 64 == 0 and sub == 2 and d["mcast"] == 1 and bx["a_box"][2] == sub
+        assert not no3d and K % 64 == 0 and sub == 2 and bx["a_box"][2] == sub
     else:
         assert bx["a_box"][2] == 1
-        assert no3d or K % 64 != 0 or sub == 1 or d["mcast"] == 2
+        assert no3d or K % 64 != 0 or sub == 1
     a_bytes = 64 * rows_a * sub * 2  # one stage of A, 3-D or one 2-D box per 64-k block
     # B
     if layout == "kn":
-        cols = 128 if swap and d["tile_n"] > 64 else (d["tile_n"] if swap else (d["mma_n"] // 2 if pair else d["mma_n"]))
+        cols = 128 if swap else (d["mma_n"] // 2 if pair else d["mma_n"])
         if bx["b_3d"]:
             assert not no3d and N >= 64 and cols % 64 == 0 and cols >= 128
             assert bx["b_box"] == [64, bk, cols // 64]
@@ -264,14 +223,14 @@ def _check_boxes(gemm_lib, M, N, K, layout, no3d=False):
             assert bx["b2_box"] == [64, bk]  # the partial chunk's 2-D boxes
         else:
             assert bx["b_box"][1] == bk and bx["b_box"][2] == 1
-            assert bx["b_box"][0] == (d["tile_n"] if swap and d["tile_n"] <= 64 else 64)
+            assert bx["b_box"][0] == 64 and bx["b2_box"] == [64, bk]
             assert no3d or N < 64 or cols % 64 != 0 or cols < 128
         b_bytes = cols * bk * 2
     else:
-        rows_b = (d["tile_n"] if d["tile_n"] <= 64 else 128) if swap else (d["mma_n"] // 2 if pair else d["mma_n"])
+        rows_b = 128 if swap else (d["mma_n"] // 2 if pair else d["mma_n"])
         assert bx["b_box"][:2] == [64, rows_b] and bx["b2_box"] == [64, rows_b]
         if bx["b_3d"]:
-            assert not no3d and K % 64 == 0 and sub == 2 and (not swap or d["tile_n"] == 128)
+            assert not no3d and K % 64 == 0 and sub == 2
             assert bx["b_box"][2] == sub
         else:
             assert bx["b_box"][2] == 1
@@ -280,9 +239,8 @@ def _check_boxes(gemm_lib, M, N, K, layout, no3d=False):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-@pytest.mark.parametrize("force", ["", "tiled256", "tiled128", "tiled64", "pair", "pair128", "pair192", "pair64",
-                                   "swap", "swapn56", "swapn8", "pair:bk128", "tiled128:c2", "swap:c2",
-                                   "tiled64:mc", "tiled128:no3d", "pair:no3d", "swap:no3d"])
+@pytest.mark.parametrize("force", ["", "tiled256", "tiled128", "tiled64", "pair", "swap", "tiled128:c2", "swap:c2",
+                                   "tiled128:no3d", "pair:no3d", "swap:no3d"])
 def test_copy_boxes_match_the_stage(gemm_lib, monkeypatch, layout, force):
     if force:
         monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)

@@ -33,7 +33,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "path", "mma_m", "mma_n", "tile_m", "tile_n", "tiles_m", "tiles_n", "num_tiles",
         "num_kb", "block_k", "group_m", "grid", "cluster", "dp_tiles", "sk_tiles", "sk_q", "sk_r",
-        "splits", "max_slots", "num_stages", "stage_bytes", "smem_bytes", "tmem_cols", "pack", "mcast")] + [
+        "splits", "max_slots", "num_stages", "stage_bytes", "smem_bytes", "tmem_cols")] + [
         ("workspace_bytes", ctypes.c_int64), ("counter_count", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
@@ -81,6 +81,8 @@ def lib():
         L.gemm_relu_host.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
         L.gemm_relu_noalloc.restype = i32
         L.gemm_relu_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+        L.gemm_relu_noalloc_check_device_error.restype = i32
+        L.gemm_relu_noalloc_check_device_error.argtypes = [vp]
         L.gemm_relu_check_device_error.restype = i32
         L.gemm_relu_check_device_error.argtypes = [vp]
         L.gemm_relu_status_string.restype = ctypes.c_char_p
@@ -250,6 +252,40 @@ def check_device_error(stream=None, device=None):
         rc = lib().gemm_relu_check_device_error(_stream_handle(stream, dev))
     if rc != GEMM_OK:
         raise GemmReluError(rc, "device")
+
+
+def gemm_relu_noalloc(a, b, c, apply_relu: bool = True, stream=None):
+    """gemm_relu through the entry point that allocates no device memory
+    (small M only; its split-K scratch is a fixed device array of the
+    library).  ``c`` must be given: this call allocates nothing."""
+    import torch
+    if a.dtype != torch.float16 or b.dtype != torch.float16 or c.dtype != torch.float16:
+        raise TypeError("a, b and c must be float16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0] or tuple(c.shape) != (a.shape[0], b.shape[1]):
+        raise ValueError(f"bad shapes {tuple(a.shape)} @ {tuple(b.shape)} -> {tuple(c.shape)}")
+    if not (a.is_cuda and b.is_cuda and c.is_cuda) or a.device != b.device or c.device != a.device:
+        raise ValueError("a, b and c must be CUDA tensors on one device")
+    if not (a.is_contiguous() and b.is_contiguous() and c.is_contiguous()):
+        raise ValueError("a, b and c must be contiguous row-major")
+    M, K = a.shape
+    N = b.shape[1]
+    with torch.cuda.device(a.device):
+        rc = lib().gemm_relu_noalloc(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                                     int(bool(apply_relu)), _stream_handle(stream, a.device))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "gemm_relu_noalloc")
+    return c
+
+
+def noalloc_check_device_error(stream=None, device=None):
+    """Synchronize ``stream`` and raise if a gemm_relu_noalloc kernel
+    reported a timed-out wait since the last check."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = lib().gemm_relu_noalloc_check_device_error(_stream_handle(stream, dev))
+    if rc != GEMM_OK:
+        raise GemmReluError(rc, "device (noalloc)")
 
 
 def shutdown():

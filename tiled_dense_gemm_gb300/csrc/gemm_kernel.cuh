@@ -44,6 +44,7 @@ constexpr int kThreads = 224;
 constexpr uint32_t kEpiThreads = 128;
 constexpr uint32_t kEpiBarrier = 1;  // named barrier id for the epilogue warps
 constexpr int kMaxStagesDev = 16;
+constexpr uint64_t kTestTimeoutNs = 1000000;  // wait limit of a launch with the test hook set (1 ms)
 constexpr uint32_t kOperandA = 128 * kBlockK * 2;  // bytes of one 128-row box of 64 k
 constexpr uint32_t kSwizzleRow = 128;              // bytes per swizzled row
 constexpr uint32_t kAtomBytes = 1024;              // 8 swizzled rows
@@ -87,37 +88,32 @@ struct KParams {
     int32_t a3d, b3d;
     uint32_t idesc;
     uint64_t timeout_ns;
+    // Test hook of the bounded waits, 0 in every normal call.  k + 1: the
+    // producers of every CTA leave k-block k of the CTA's first work item
+    // uncopied (its stage is still armed for the bytes), so the MMA warp's
+    // wait for that stage runs out; the host pairs it with a short
+    // timeout_ns and a plan without clusters.
+    int32_t test_drop_kb;
     uint16_t* C;          // 16-bit words of C (binary16 or bfloat16)
     float* ws;            // stream-K partial tiles: [sk_tile][slot][col][128 lanes]
     uint32_t* counters;   // stream-K arrivals, one per stream-K tile, zero between launches
     int32_t* err;         // first error code of the launch (0 = none)
 };
 
-// kMode 0: C tile 128 x 256; 1: C tile 128 x 128; 2: swapped operands
-// (C tile mpad x 128: B^T is the MMA A operand, A^T the MMA B operand);
-// 3: CTA pair, C tile 256 x 256 (each CTA holds 128 rows of A, 128 columns
-// of B, and accumulates its 128 rows x 256 columns); 4: CTA pair, C tile
-// 256 x 128 (each CTA holds 128 rows of A and 64 columns of B); 5: C tile
-// 128 x 64; 6: CTA pair, C tile 256 x 192 (each CTA holds 96 columns of B:
-// one 64-wide chunk and a half-filled one, whose 32 columns come through a
-// second tensor map of B when B is stored (K, N)); 7: CTA pair, C tile
-// 256 x 64 (each CTA holds 32 columns of B, a half-filled chunk); 8: as 3,
-// with ring stages of 128 k-rows (8 MMAs per stage instead of 4).
+// kMode 0: C tile 128 x 256; 1: C tile 128 x 128; 5: C tile 128 x 64;
+// 2: swapped operands (C tile mpad x 128: B^T is the MMA A operand, A^T the
+// MMA B operand); 3: CTA pair, C tile 256 x 256 (each CTA holds 128 rows of
+// A and 128 columns of B, and accumulates its 128 rows x 256 columns).
 template <int kMode>
 struct ModeTraits {
+    static_assert(kMode == 0 || kMode == 1 || kMode == 2 || kMode == 3 || kMode == 5, "unknown kernel mode");
     static constexpr bool kSwap = (kMode == 2);
-    static constexpr bool kPair = (kMode == 3 || kMode == 4 || kMode == 6 || kMode == 7 || kMode == 8);
+    static constexpr bool kPair = (kMode == 3);
     static constexpr int kCG = kPair ? 2 : 1;
-    static constexpr uint32_t kBN = (kMode == 5 || kMode == 7)   ? 64
-                                    : (kMode == 1 || kMode == 4) ? 128
-                                    : (kMode == 6)               ? 192
-                                                                 : 256;  // C columns per tile
+    static constexpr uint32_t kBN = (kMode == 5) ? 64 : (kMode == 1) ? 128 : 256;  // C columns per tile
     static constexpr uint32_t kTileM = kPair ? 256 : 128;      // C rows per tile (normal)
     static constexpr uint32_t kBCols = kPair ? kBN / 2 : kBN;  // B columns loaded per CTA
-    // (K, N) storage: full 64-wide chunks of B per CTA, and the width of a
-    // last partial one (0 if none)
-    static constexpr uint32_t kBFull = kBCols / 64, kBRem = kBCols % 64;
-    static constexpr uint32_t kBChunks = kBFull + (kBRem ? 1 : 0);
+    static constexpr uint32_t kBChunks = kBCols / 64;          // their 64-wide chunks (B stored (K, N))
     // k-rows per ring stage (the plan's block_k): 128 (8 MMAs per stage, so
     // that the MMA warp's fixed per-stage work -- barrier wait, fence,
     // commit -- is paid once per 8 MMAs), except for the 256-column tiles:
@@ -196,8 +192,8 @@ struct Producer {
     Ctrl* ctrl;
     const CUtensorMap* tmA;
     const CUtensorMap* tmB;
-    // second map of B (K, N): boxes of a pair CTA's last partial chunk
-    // (256 x 192), or 64-column 2-D boxes when tmB is a 3-D map
+    // second map of B (K, N): 64-column 2-D boxes, for the columns a 3-D
+    // map of whole chunks leaves out
     const CUtensorMap* tmB2;
     gemm_relu_plan_t pl;
     uint32_t stages, stride, a_bytes, rank, S, full0, empty0, tx_bytes;
@@ -213,11 +209,11 @@ struct Producer {
     uint64_t pol_first;
     uint32_t a_sub_bytes;  // swapped: bytes of one 64-k box of A's padded rows
     bool b_nk;             // B stored (N, K): its boxes are (64 k) x (rows of N)
-    uint32_t b_sub_bytes;  // swapped, B stored (N, K): bytes of one 64-k box of the tile's B rows
-    bool mc;               // A multicast: this CTA fetches box `rank` of each A stage for both CTAs
     bool a3d, b3d;         // one 3-D copy per operand and stage (see KParams)
     bool b_edge;           // B (K, N), b3d: this item's columns reach past the 3-D map's whole chunks
     int32_t part;          // copies this thread issues: 0 all, 1 A's (and arms each stage), 2 B's
+    int32_t items;         // work items begun
+    int32_t drop_kb;       // test hook: k-block of the first item not copied (-1: none)
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
@@ -232,14 +228,14 @@ struct Producer {
         tx_bytes = (T::kPair ? 2u : 1u) * (uint32_t)pl.stage_bytes;
         a_sub_bytes = (uint32_t)pl.tile_m * kSwizzleRow;
         b_nk = p_.b_kmajor != 0;
-        b_sub_bytes = (pl.tile_n <= 64 ? 64u : 128u) * kSwizzleRow;
         once_a = pl.tiles_n == 1;
         once_b = pl.tiles_m == 1;
-        mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
         a3d = p_.a3d != 0;
         b3d = p_.b3d != 0;
         b_edge = false;
         part = part_;
+        items = 0;
+        drop_kb = p_.test_drop_kb - 1;
         pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
     }
@@ -289,18 +285,11 @@ struct Producer {
             tma_load_3d_pair(dst, m, bar, 0, y, z);
     }
 
-    template <bool kPre>
-    __device__ __forceinline__ void ld_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int32_t x, int32_t y) {
-        if constexpr (kPre)
-            tma_prefetch_2d(m, x, y);
-        else
-            tma_load_2d_mcast(dst, m, bar, x, y, 0x3);
-    }
-
     // Move to the next work item; false when there is none.
     __device__ __forceinline__ bool next_item() {
         if (!wi.next(pl, w)) return false;
         have_item = true;
+        ++items;
         kb = w.kb0;
         // first row of A and first column of B this CTA loads
         if constexpr (T::kPair) {
@@ -314,7 +303,7 @@ struct Producer {
             b_col = w.tn * pl.tile_n;
         }
         {
-            constexpr int32_t kChunks = T::kSwap ? 2 : (int32_t)(T::kPair ? T::kBCols : T::kBN) / 64;
+            constexpr int32_t kChunks = T::kSwap ? 2 : (int32_t)T::kBChunks;
             b_edge = b_col / 64 + kChunks > (int32_t)(p.N / 64);
         }
         return true;
@@ -353,11 +342,7 @@ struct Producer {
                     ld_pair<kPre>(a_dst + i * kOperandA, tmA, full_leader, k0 + (int32_t)(i * kBlockK), a_row);
             }
         } else if constexpr (!T::kSwap) {
-            if (T::kSub == 2 && mc) {
-                // one of the stage's two A boxes; the peer fetches the other,
-                // and each lands in both CTAs
-                ld_mc<kPre>(a_dst + rank * kOperandA, tmA, full, k0 + (int32_t)(rank * kBlockK), a_row);
-            } else if (a3d) {
+            if (a3d) {
                 ld3<kPre>(a_dst, tmA, full, a_row, k0 / kBlockK, once_a);
             } else {
 #pragma unroll
@@ -392,25 +377,16 @@ struct Producer {
                         ld_pair<kPre>(b_dst + i * T::kBCols * kSwizzleRow, tmB, full_leader,
                                       k0 + (int32_t)(i * kBlockK), b_col);
                 }
-            } else if (T::kBRem == 0 && b3d && !b_edge) {
+            } else if (b3d && !b_edge) {
                 // all of this CTA's 64-column chunks in one copy
                 ld3_pair<kPre>(b_dst, tmB, full_leader, k0, b_col / 64);
-            } else if (T::kBRem == 0 && b3d) {
-                // the partial last chunk: 2-D boxes through the second map
-                if constexpr (T::kBFull > 0) {
-#pragma unroll
-                    for (uint32_t j = 0; j < T::kBFull; ++j)
-                        ld_pair<kPre>(b_dst + j * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)j, k0);
-                }
             } else {
-                if constexpr (T::kBFull > 0) {
+                // one 2-D box per chunk (b3d: the columns reach the partial
+                // last chunk, through the second map)
+                const CUtensorMap* m2 = b3d ? tmB2 : tmB;
 #pragma unroll
-                    for (uint32_t j = 0; j < T::kBFull; ++j)
-                        ld_pair<kPre>(b_dst + j * kBChunk, tmB, full_leader, b_col + 64 * (int32_t)j, k0);
-                }
-                if constexpr (T::kBRem != 0)
-                    ld_pair<kPre>(b_dst + T::kBFull * kBChunk, tmB2, full_leader, b_col + 64 * (int32_t)T::kBFull,
-                                  k0);
+                for (uint32_t j = 0; j < T::kBChunks; ++j)
+                    ld_pair<kPre>(b_dst + j * kBChunk, m2, full_leader, b_col + 64 * (int32_t)j, k0);
             }
         } else if constexpr (!T::kSwap) {
             if (b_nk && b3d) {
@@ -432,8 +408,8 @@ struct Producer {
                     ld<kPre>(b_dst + j * kBChunk, m2, full, b_col + 64 * (int32_t)j, k0, once_b);
             }
         } else {
-            // MMA A operand: the tile's columns of B, one 64-wide chunk of kBK
-            // k-rows per TMA box (a narrow tile fills part of one chunk)
+            // MMA A operand: the tile's 128 columns of B, one 64-wide chunk of
+            // kBK k-rows per TMA box
             if (b3d && (b_nk || !b_edge)) {
                 // one copy: the tile's B rows (B stored (N, K)) for every
                 // 64 k, or both 64-column chunks (B (K, N))
@@ -449,10 +425,10 @@ struct Producer {
                 // B stored (N, K): the tile's B rows, one K-major box per 64 k
 #pragma unroll
                 for (uint32_t i = 0; i < T::kBK / kBlockK; ++i)
-                    ld<kPre>(a_dst + i * b_sub_bytes, tmB, full, k0 + (int32_t)(i * kBlockK), b_col, once_b);
+                    ld<kPre>(a_dst + i * 128u * kSwizzleRow, tmB, full, k0 + (int32_t)(i * kBlockK), b_col, once_b);
             } else {
                 ld<kPre>(a_dst, tmB, full, b_col, k0, once_b);
-                if (pl.tile_n > 64) ld<kPre>(a_dst + kBChunk, tmB, full, b_col + 64, k0, once_b);
+                ld<kPre>(a_dst + kBChunk, tmB, full, b_col + 64, k0, once_b);
             }
         }
     }
@@ -474,8 +450,10 @@ struct Producer {
             const uint32_t a_dst = stages + s * stride;
             const uint32_t b_dst = a_dst + a_bytes;
             const int32_t k0 = kb * (int32_t)T::kBK;
-            if (part != 2) copies_a<kPre>(full, a_dst, b_dst, k0);
-            if (part != 1) copies_b<kPre>(full, a_dst, b_dst, k0);
+            if (kPre || kb != drop_kb || items != 1) {
+                if (part != 2) copies_a<kPre>(full, a_dst, b_dst, k0);
+                if (part != 1) copies_b<kPre>(full, a_dst, b_dst, k0);
+            }
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -513,7 +491,7 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
     uint64_t a_desc0, b_desc0;
     uint32_t a_off[kK], b_off[kK];
     if constexpr (T::kSwap) {
-        const uint32_t a_box16 = ((pl.tile_n <= 64 ? 64u : 128u) * kSwizzleRow) >> 4;
+        const uint32_t a_box16 = (128u * kSwizzleRow) >> 4;  // one 64-k box of the tile's B rows
         const uint32_t b_box16 = ((uint32_t)pl.tile_m * kSwizzleRow) >> 4;  // one 64-k box of A's rows
         a_desc0 = b_nk ? make_sw128_desc(stages, 16, kAtomBytes)
                        : make_sw128_desc(stages, T::kBK * kSwizzleRow, kAtomBytes);
@@ -538,7 +516,6 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
         }
     }
     const uint32_t stride16 = stride >> 4;
-    const bool mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
     WorkIter wi;
     wi.init(pl, worker, (int32_t)rank);
     WorkItem w;
@@ -564,12 +541,8 @@ __device__ __forceinline__ void mma_role(const KParams& p, Ctrl* ctrl, uint32_t 
 #pragma unroll
             for (uint32_t k = 0; k < kK; ++k)
                 mma_f16_ss<T::kCG>(d_tmem, a_desc + a_off[k], b_desc + b_off[k], idesc, k > 0 ? 1u : acc);
-            // stage free (in both CTAs of a pair, or of an A-multicast
-            // cluster, whose peer writes into this stage) once these MMAs are done
-            if (mc)
-                mma_commit_mcast(empty0 + 8u * s, 0x3);
-            else
-                mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
+            // stage free (in both CTAs of a pair) once these MMAs are done
+            mma_commit<T::kCG>(empty0 + 8u * s, 0x3);
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
@@ -663,12 +636,9 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t quarter = warp & 3u;  // TMEM lanes a warp may access: 32 * (warp % 4) ...
     const uint32_t lane_row = quarter * 32 + lane;  // TMEM lane = accumulator row
-    // swapped: the C column (within the tile) of this lane.  An M = 128 MMA
-    // puts accumulator row r in lane r; an M = 64 MMA (narrow tiles) puts it
-    // in lane (r / 16) * 32 + r % 16, leaving lanes 16..31 of each quarter
-    // unused (column past any tile).
-    const int32_t swap_col = pl.tile_n > 64 ? (int32_t)lane_row
-                                            : (lane < 16 ? (int32_t)(quarter * 16 + lane) : 1 << 30);
+    // swapped: the C column (within the tile) of this lane (the M = 128 MMA
+    // puts accumulator row r in lane r)
+    const int32_t swap_col = (int32_t)lane_row;
     const uint32_t half = T::kPair ? rank : 0u;      // which 128 rows of a pair tile
     const uint32_t cols_per_buf = (uint32_t)pl.tmem_cols / 2;
     const uint32_t ncols = (uint32_t)pl.mma_n;
@@ -1132,25 +1102,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = smem_u32(smem);
     const uint32_t stages = (base + (uint32_t)sizeof(Ctrl) + 1023u) & ~1023u;
     const gemm_relu_plan_t& pl = p.plan;
-    // MMA A operand per stage: 128 rows of 64 k; swapped, one 64-wide chunk
-    // of B columns (kBK k-rows) per 64 tile columns (a narrow tile, at most
-    // 64 columns, takes one chunk and an M = 64 MMA)
-    const uint32_t a_bytes = T::kSwap ? (pl.tile_n <= 64 ? 1u : 2u) * T::kBK * kSwizzleRow : T::kSub * kOperandA;
+    // MMA A operand per stage: 128 rows of 64 k; swapped, the tile's two
+    // 64-wide chunks of B columns (kBK k-rows each)
+    const uint32_t a_bytes = T::kSwap ? 2u * T::kBK * kSwizzleRow : T::kSub * kOperandA;
     const uint32_t b_bytes = (T::kPair ? T::kBChunks * T::kBK * kSwizzleRow
                                        : ((uint32_t)pl.mma_n * T::kBK * 2 + 1023u) & ~1023u);
     const uint32_t stride = a_bytes + b_bytes;
     const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // CTA pairs (one MMA for two CTAs), cluster split-K and A multicast run
-    // in clusters
-    const bool mc = !T::kPair && !T::kSwap && T::kSub == 2 && pl.mcast > 1;
-    const bool clustered = T::kPair || cluster_split(pl) || mc;
+    // CTA pairs (one MMA for two CTAs) and cluster split-K run in clusters
+    const bool clustered = T::kPair || cluster_split(pl);
     const uint32_t rank = clustered ? cluster_ctarank() : 0u;
     const int32_t worker = clustered ? (int32_t)(blockIdx.x / (uint32_t)pl.cluster) : (int32_t)blockIdx.x;
-    // A 3-D tensor map must only meet the 3-D copies issued for it: B (K, N)
-    // as whole 64-column chunks (no partial chunk per CTA), a swapped tile
-    // 128 columns wide, and no A multicast (its copies are 2-D).  Every CTA
-    // decides alike, before any barrier.
-    if ((p.b3d && ((!p.b_kmajor && T::kBRem != 0) || (T::kSwap && pl.tile_n != 128))) || (p.a3d && mc)) {
+    // The plan must be one this kernel shape was built for (the host never
+    // builds another): swapped tiles 128 columns wide, tiled and paired
+    // tiles of the kernel's width.  Every CTA decides alike, before any
+    // barrier.
+    if ((T::kSwap && pl.tile_n != 128) || (!T::kSwap && (uint32_t)pl.mma_n != T::kBN)) {
         if (threadIdx.x == 0) atomicCAS(p.err, 0, kErrConfig);
         return;
     }
@@ -1158,12 +1125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if constexpr (T::kBRem != 0) tma_prefetch_desc(&tmB2);
         if constexpr (!T::kSwap) tma_prefetch_desc(&tmC);
         for (int s = 0; s < pl.num_stages; ++s) {
             mbar_init(smem_u32(&ctrl->full[s]), 1);
-            // A multicast: both CTAs' MMAs free a stage (the peer writes into it)
-            mbar_init(smem_u32(&ctrl->empty[s]), mc ? 2u : 1u);
+            mbar_init(smem_u32(&ctrl->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctrl->tmem_full[b]), 1);

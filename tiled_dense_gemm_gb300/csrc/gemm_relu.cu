@@ -17,25 +17,6 @@
 namespace gr {
 
 // C := +0 for K == 0 (the empty sum).
-// Copy of an operand's rows to a 128-byte-aligned row pitch (16-byte
-// vectors; pitches in vectors).  blockIdx.y selects the operand.
-struct PackJob {
-    const uint4* src;
-    uint4* dst;
-    int64_t rows, row_vecs, src_pitch, dst_pitch;
-};
-
-__global__ void pack_rows_kernel(PackJob a, PackJob b) {
-    grid_launch_dependents();
-    grid_dependency_wait();  // the operands may come from the previous kernel
-    const PackJob& j = blockIdx.y == 0 ? a : b;
-    for (int64_t r = blockIdx.x; r < j.rows; r += gridDim.x) {
-        const uint4* src = j.src + r * j.src_pitch;
-        uint4* dst = j.dst + r * j.dst_pitch;
-        for (int64_t c = threadIdx.x; c < j.row_vecs; c += blockDim.x) dst[c] = src[c];
-    }
-}
-
 __global__ void zero_fill_kernel(uint4* c, int64_t n16) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
@@ -53,8 +34,6 @@ struct StreamBuffers {
     size_t ws_bytes = 0;
     uint32_t* counters = nullptr;  // split-K arrival counters + ready flags (zero between launches)
     size_t counter_bytes = 0;
-    void* packed = nullptr;  // operands copied to a 128-byte row pitch
-    size_t packed_bytes = 0;
     void* hA = nullptr;  // staging for the host-buffer entry point
     void* hB = nullptr;
     void* hC = nullptr;
@@ -68,7 +47,7 @@ struct DeviceState {
     int sm_count = 0;
     int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
     int32_t* d_err = nullptr;
-    bool attr_set[9] = {false, false, false, false, false, false, false, false, false};
+    bool attr_set[6] = {false, false, false, false, false, false};  // per kernel mode
     std::vector<StreamBuffers> streams;
 };
 
@@ -197,9 +176,9 @@ int grow(void** buf, size_t* have, size_t need, cudaStream_t stream, bool zero) 
 }
 
 int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool bf16, uint64_t pitch_elems = 0) {
+              uint32_t box_outer, bool bf16) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {(pitch_elems ? pitch_elems : inner) * 2};  // bytes between rows
+    cuuint64_t strides[1] = {inner * 2};  // bytes between rows
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -255,9 +234,8 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     unsigned n_attr = 1;
-    // CTA pairs and cluster split-K: `cluster` CTAs per worker; A multicast:
-    // clusters of `mcast` one-CTA workers
-    const unsigned cdim = (unsigned)pl.cluster * (pl.mcast > 1 ? (unsigned)pl.mcast : 1u);
+    // CTA pairs and cluster split-K: `cluster` CTAs per worker
+    const unsigned cdim = (unsigned)pl.cluster;
     if (cdim > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = cdim;
@@ -290,6 +268,78 @@ int check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N
     return GEMM_OK;
 }
 
+// The tensor maps of one call: A, B (and B's second, 2-D map), C.
+struct Maps {
+    CUtensorMap ta, tb, tb2, tc;
+    int32_t a3d, b3d;
+};
+
+int encode_maps(const gemm_relu_plan_t& pl, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                int64_t K, bool b_nk, bool bf16, const char* force, Maps* m) {
+    // the boxes of one stage's copies (3-D where the shapes allow)
+    gemm_relu_boxes_t bx;
+    int rc = plan_boxes(pl, M, N, K, b_nk, force, &bx);
+    if (rc != GEMM_OK) return rc;
+    if (bx.a_3d)
+        rc = encode_3d(&m->ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[1], bx.a_box[2], bf16, 0);
+    else
+        rc = encode_2d(&m->ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[0], bx.a_box[1], bf16);
+    if (rc != GEMM_OK) return rc;
+    m->a3d = bx.a_3d;
+    if (!b_nk) {
+        // the second map: 64-column 2-D boxes (the partial chunk a 3-D view
+        // of whole chunks leaves out)
+        rc = encode_2d(&m->tb2, B, (uint64_t)N, (uint64_t)K, bx.b2_box[0], bx.b2_box[1], bf16);
+        if (rc == GEMM_OK) {
+            if (bx.b_3d)
+                rc = encode_3d(&m->tb, B, (uint64_t)bx.b_view_inner, (uint64_t)K, bx.b_box[1], bx.b_box[2], bf16,
+                               (uint64_t)N);
+            else
+                rc = encode_2d(&m->tb, B, (uint64_t)N, (uint64_t)K, bx.b_box[0], bx.b_box[1], bf16);
+        }
+    } else {
+        rc = encode_2d(&m->tb2, B, (uint64_t)K, (uint64_t)N, bx.b2_box[0], bx.b2_box[1], bf16);
+        if (rc == GEMM_OK) {
+            if (bx.b_3d)
+                rc = encode_3d(&m->tb, B, (uint64_t)K, (uint64_t)N, bx.b_box[1], bx.b_box[2], bf16, 0);
+            else
+                m->tb = m->tb2;
+        }
+    }
+    if (rc != GEMM_OK) return rc;
+    m->b3d = bx.b_3d;
+    // C: 64-column x 32-row boxes, one per epilogue warp and chunk
+    return encode_2d(&m->tc, C, (uint64_t)N, (uint64_t)M, 64, 32, bf16);
+}
+
+// Encoded tensor maps per (pointers, shape, B layout, element type): a map
+// holds only an address, sizes, strides and box shapes, so it stays valid
+// for any call with the same arguments, whatever the buffers hold.
+struct MapKey {
+    const void* A;
+    const void* B;
+    const void* C;
+    int64_t M, N, K;
+    int32_t flags;
+    bool operator==(const MapKey& o) const {
+        return A == o.A && B == o.B && C == o.C && M == o.M && N == o.N && K == o.K && flags == o.flags;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = (uint64_t)(uintptr_t)k.A * 0x9E3779B97F4A7C15ull;
+        h ^= (uint64_t)(uintptr_t)k.B + 0x7F4A7C159E3779B9ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)(uintptr_t)k.C + 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.M + 0xBF58476D1CE4E5B9ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.N + 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.K + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.flags + (h << 6) + (h >> 2);
+        return (size_t)h;
+    }
+};
+constexpr size_t kMapCacheEntries = 1024;
+std::unordered_map<MapKey, Maps, MapKeyHash> g_maps[kMaxDevices];
+
 int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                int apply_relu, bool b_nk, bool bf16, cudaStream_t st, int dev) {
     DeviceState& d = g_dev[dev];
@@ -304,8 +354,9 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     }
     gemm_relu_plan_t pl;
     const char* force = getenv("GEMM_RELU_FORCE_PATH");
-    if (force && *force) {
-        // tuning / test override: plan every call, bypass the cache
+    const bool forced = force && *force;
+    if (forced) {
+        // tuning / test override: plan every call, bypass the caches
         int rc = plan_problem(M, N, K, d.sm_count, d.max_pairs, force, &pl);
         if (rc != GEMM_OK) return rc;
     } else {
@@ -321,6 +372,8 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
             cache.emplace(key, pl);
         }
     }
+    // the swapped kernel's exchange buffer holds one peer's partial
+    if (pl.path == 3 && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
     KParams kp;
     memset(&kp, 0, sizeof(kp));
     kp.plan = pl;
@@ -334,6 +387,16 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     kp.err = d.d_err;
     // generous bound: 2 s plus 2 us per k-block of the longest wait
     kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
+    {
+        // test hook of the bounded waits (see KParams::test_drop_kb)
+        const char* drop = getenv("GEMM_RELU_TEST_DROP_KB");
+        if (drop && *drop) {
+            const long kb = strtol(drop, nullptr, 10);
+            if (kb < 0 || kb >= pl.num_kb || pl.cluster != 1) return GEMM_ERR_INVALID_ARG;
+            kp.test_drop_kb = (int32_t)kb + 1;
+            kp.timeout_ns = kTestTimeoutNs;
+        }
+    }
     if (pl.sk_tiles > 0) {
         StreamBuffers& sb = buffers_for_locked(d, st);
         int rc = grow(reinterpret_cast<void**>(&sb.ws), &sb.ws_bytes, (size_t)pl.workspace_bytes, st, false);
@@ -345,111 +408,35 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         kp.ws = sb.ws;
         kp.counters = sb.counters;
     }
-    // operands whose row pitch is not a multiple of 128 bytes: copy them to
-    // a 128-byte pitch first when the plan says it pays
-    uint64_t a_pitch = 0, b_pitch = 0;  // elements; 0 = as stored
-    if (pl.pack) {
-        const uint64_t b_rows = b_nk ? (uint64_t)N : (uint64_t)K, b_len = b_nk ? (uint64_t)K : (uint64_t)N;
-        const bool pa = (K % 64) != 0, pb = (b_len % 64) != 0;
-        if (pa || pb) {
-            const uint64_t ap = ((uint64_t)K + 63) / 64 * 64, bp = (b_len + 63) / 64 * 64;
-            const size_t a_bytes = pa ? (size_t)M * ap * 2 : 0, b_bytes = pb ? (size_t)b_rows * bp * 2 : 0;
-            StreamBuffers& sb = buffers_for_locked(d, st);
-            int rc = grow(&sb.packed, &sb.packed_bytes, a_bytes + b_bytes, st, false);
-            if (rc != GEMM_OK) return rc;
-            uint8_t* pbuf = static_cast<uint8_t*>(sb.packed);
-            PackJob ja = {reinterpret_cast<const uint4*>(A), reinterpret_cast<uint4*>(pbuf), pa ? M : 0,
-                          (int64_t)K / 8, (int64_t)K / 8, (int64_t)ap / 8};
-            PackJob jb = {reinterpret_cast<const uint4*>(B), reinterpret_cast<uint4*>(pbuf + a_bytes),
-                          pb ? (int64_t)b_rows : 0, (int64_t)b_len / 8, (int64_t)b_len / 8, (int64_t)bp / 8};
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            const int64_t most = pa && pb ? (M > (int64_t)b_rows ? M : (int64_t)b_rows) : (pa ? M : (int64_t)b_rows);
-            cfg.gridDim = dim3((unsigned)(most < (int64_t)d.sm_count * 8 ? most : (int64_t)d.sm_count * 8), 2, 1);
-            cfg.blockDim = dim3(256, 1, 1);
-            cfg.stream = st;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&cfg, pack_rows_kernel, ja, jb) != cudaSuccess) {
-                cudaGetLastError();
-                return GEMM_ERR_LAUNCH;
-            }
-            if (pa) {
-                A = pbuf;
-                a_pitch = ap;
-            }
-            if (pb) {
-                B = pbuf + a_bytes;
-                b_pitch = bp;
-            }
-        }
-    }
-    CUtensorMap ta, tb;
-    const bool swap = (pl.path == 3);
-    // the swapped kernel's exchange buffer holds one peer's partial
-    if (swap && cluster_split(pl) && pl.cluster != 2) return GEMM_ERR_INVALID_ARG;
-    // A multicast pairs column-neighbour tiles of the 128 x 64 / 128 x 128 kernels
-    if (pl.mcast > 1 && (pl.mcast != 2 || pl.path != 2 || (pl.mma_n != 64 && pl.mma_n != 128) ||
-                         pl.block_k != 2 * kBlockK || pl.cluster != 1 || pl.tiles_n % 2 != 0 ||
-                         pl.grid % 2 != 0 || pl.dp_tiles != pl.num_tiles))
-        return GEMM_ERR_INVALID_ARG;
-    // the boxes of one stage's copies (3-D where the shapes allow)
-    gemm_relu_boxes_t bx;
-    int rc = plan_boxes(pl, M, N, K, b_nk, force, &bx);
-    if (rc != GEMM_OK) return rc;
-    if (bx.a_3d)
-        rc = encode_3d(&ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[1], bx.a_box[2], bf16, a_pitch);
-    else
-        rc = encode_2d(&ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[0], bx.a_box[1], bf16, a_pitch);
-    if (rc != GEMM_OK) return rc;
-    kp.a3d = bx.a_3d;
-    CUtensorMap tb2;
-    if (!b_nk) {
-        // the second map: 2-D boxes (a pair CTA's partial chunk, or the
-        // partial chunk a 3-D view leaves out)
-        rc = encode_2d(&tb2, B, (uint64_t)N, (uint64_t)K, bx.b2_box[0], bx.b2_box[1], bf16, b_pitch);
-        if (rc == GEMM_OK) {
-            if (bx.b_3d)
-                rc = encode_3d(&tb, B, (uint64_t)bx.b_view_inner, (uint64_t)K, bx.b_box[1], bx.b_box[2], bf16,
-                               b_pitch ? b_pitch : (uint64_t)N);
-            else
-                rc = encode_2d(&tb, B, (uint64_t)N, (uint64_t)K, bx.b_box[0], bx.b_box[1], bf16, b_pitch);
-        }
+    Maps local;
+    const Maps* m = &local;
+    if (forced) {
+        int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, force, &local);
+        if (rc != GEMM_OK) return rc;
     } else {
-        rc = encode_2d(&tb2, B, (uint64_t)K, (uint64_t)N, bx.b2_box[0], bx.b2_box[1], bf16, b_pitch);
-        if (rc == GEMM_OK) {
-            if (bx.b_3d)
-                rc = encode_3d(&tb, B, (uint64_t)K, (uint64_t)N, bx.b_box[1], bx.b_box[2], bf16, b_pitch);
-            else
-                tb = tb2;
+        auto& cache = g_maps[dev];
+        const MapKey key{A, B, C, M, N, K, (b_nk ? 1 : 0) | (bf16 ? 2 : 0)};
+        auto it = cache.find(key);
+        if (it == cache.end()) {
+            int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, nullptr, &local);
+            if (rc != GEMM_OK) return rc;
+            if (cache.size() >= kMapCacheEntries) cache.clear();
+            it = cache.emplace(key, local).first;
         }
+        m = &it->second;
     }
-    if (rc != GEMM_OK) return rc;
-    kp.b3d = bx.b_3d;
-    // C: 64-column x 32-row boxes, one per epilogue warp and chunk
-    CUtensorMap tc;
-    rc = encode_2d(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32, bf16);
-    if (rc != GEMM_OK) return rc;
-    if (swap) {
-        // a narrow tile (<= 64 columns) runs M = 64 MMAs; B^T is MN-major
-        // when B is stored (K, N)
-        kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/!b_nk,
-                                      /*b_mn=*/false, bf16);
-        return launch_mode<2>(d, pl, kp, ta, tb, tb2, tc, st);
+    kp.a3d = m->a3d;
+    kp.b3d = m->b3d;
+    if (pl.path == 3) {
+        // M = 128 tile columns; B^T is MN-major when B is stored (K, N)
+        kp.idesc = make_idesc_f16_f32(128u, (uint32_t)pl.mma_n, /*a_mn=*/!b_nk, /*b_mn=*/false, bf16);
+        return launch_mode<2>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/!b_nk, bf16);
-    if (pl.path == 4) {
-        if (pl.mma_n == 128) return launch_mode<4>(d, pl, kp, ta, tb, tb2, tc, st);
-        if (pl.mma_n == 192) return launch_mode<6>(d, pl, kp, ta, tb, tb2, tc, st);
-        if (pl.mma_n == 64) return launch_mode<7>(d, pl, kp, ta, tb, tb2, tc, st);
-        if (pl.block_k == 2 * kBlockK) return launch_mode<8>(d, pl, kp, ta, tb, tb2, tc, st);
-        return launch_mode<3>(d, pl, kp, ta, tb, tb2, tc, st);
-    }
-    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, ta, tb, tb2, tc, st);
-    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, ta, tb, tb2, tc, st);
-    return launch_mode<1>(d, pl, kp, ta, tb, tb2, tc, st);
+    if (pl.path == 4) return launch_mode<3>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
+    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
+    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
+    return launch_mode<1>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
 }
 
 // A launch gave up part-way (the error word is set): clear it and every
@@ -591,7 +578,6 @@ extern "C" void gemm_relu_shutdown(void) {
             for (auto& s : d.streams) {
                 cudaFree(s.ws);
                 cudaFree(s.counters);
-                cudaFree(s.packed);
                 cudaFree(s.hA);
                 cudaFree(s.hB);
                 cudaFree(s.hC);
@@ -601,6 +587,7 @@ extern "C" void gemm_relu_shutdown(void) {
         }
         d = DeviceState();
         g_plans[dev].clear();
+        g_maps[dev].clear();
     }
     if (have_dev) cudaSetDevice(prev);
     cudaGetLastError();

@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -139,16 +140,17 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     gemm_relu_plan_t pl;
     rc = plan_problem(M, N, K, s.sm_count, -1, "swap", &pl);  // no clusters: plain launch
     if (rc != GEMM_OK) return rc;
-    if (pl.path != 3 || pl.cluster != 1 || pl.mcast != 1) return GEMM_ERR_TOO_LARGE;
+    if (pl.path != 3 || pl.cluster != 1) return GEMM_ERR_TOO_LARGE;
     const size_t partial_bytes = (size_t)pl.workspace_bytes;
     if ((size_t)pl.counter_count * (1 + (size_t)pl.max_slots) > kMaxCounters ||
         partial_bytes > kScratchBytes - kPartialOffset)
         return GEMM_ERR_TOO_LARGE;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // The array keeps whatever the previous call left: the error word and
-    // the counters must start at zero (partials are written before read).
-    if (cudaMemsetAsync(s.scratch, 0, kPartialOffset, st) != cudaSuccess) {
+    // The array keeps whatever the previous call left: the counters must
+    // start at zero (partials are written before they are read).  The error
+    // word is left as it is, for gemm_relu_noalloc_check_device_error.
+    if (cudaMemsetAsync(s.scratch + kCounterOffset, 0, kPartialOffset - kCounterOffset, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -165,17 +167,54 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     kp.counters = reinterpret_cast<uint32_t*>(s.scratch + kCounterOffset);
     kp.ws = reinterpret_cast<float*>(s.scratch + kPartialOffset);
     kp.timeout_ns = 2000000000ull + 2000ull * (uint64_t)pl.num_kb;
-    kp.idesc = make_idesc_f16_f32(pl.tile_n <= 64 ? 64u : 128u, (uint32_t)pl.mma_n, /*a_mn=*/true,
-                                  /*b_mn=*/false);
+    {
+        // the test hook of the bounded waits, as in gemm_relu
+        const char* drop = getenv("GEMM_RELU_TEST_DROP_KB");
+        if (drop && *drop) {
+            const long kb = strtol(drop, nullptr, 10);
+            if (kb < 0 || kb >= pl.num_kb) return GEMM_ERR_INVALID_ARG;
+            kp.test_drop_kb = (int32_t)kb + 1;
+            kp.timeout_ns = kTestTimeoutNs;
+        }
+    }
+    kp.idesc = make_idesc_f16_f32(128u, (uint32_t)pl.mma_n, /*a_mn=*/true, /*b_mn=*/false);
 
     CUtensorMap ta, tb, tc;
     if ((rc = encode(&ta, A, (uint64_t)K, (uint64_t)M, kBlockK, (uint32_t)pl.tile_m)) != GEMM_OK) return rc;
-    if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 64u,
-                     (uint32_t)pl.block_k)) != GEMM_OK)
-        return rc;
+    if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, 64u, (uint32_t)pl.block_k)) != GEMM_OK) return rc;
     if ((rc = encode(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32)) != GEMM_OK) return rc;  // unused by this kernel
 
     gemm_relu_kernel<2><<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, tb, tc, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
+}
+
+extern "C" int gemm_relu_noalloc_check_device_error(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    int rc = setup_locked(dev);
+    if (rc != GEMM_OK) return rc;
+    NoAllocState& s = g_na[dev];
+    int32_t err = 0;
+    if (cudaMemcpy(&err, s.scratch, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (err == 0) return GEMM_OK;
+    // a launch gave up part-way: clear the word and the counters it may
+    // have left set
+    if (cudaMemsetAsync(s.scratch, 0, kPartialOffset, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_ERR_TIMEOUT;
 }

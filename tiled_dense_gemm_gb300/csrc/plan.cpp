@@ -37,26 +37,11 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
     // measured: ~1 us of handshake + the peer's 128 x mma_n fp32 tile at
     // ~32 B/clk over DSMEM, plus the cluster teardown
     c.exchange = 1.0 + 128.0 * mma_n * 4.0 / 32000.0;
-    if (path == 4 && mma_n >= 256) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
+    if (path == 4) {  // CTA pair, 256 x 256 (each CTA 128 x 256)
         c.kb = 0.29;
         c.tile_store = 2.5;
         c.partial = 3.0;           // measured: ~3 us to publish a 128 KiB partial
         c.reduce_per_slot = 3.0;
-    } else if (path == 4 && mma_n == 192) {  // CTA pair, 256 x 192: measured no faster per
-        c.kb = 0.32;                          // k-block than 256 x 256 (the MMA warp's loop bounds both)
-        c.tile_store = 1.9;
-        c.partial = 4.5;
-        c.reduce_per_slot = 3.0;
-    } else if (path == 4 && mma_n == 64) {  // CTA pair, 256 x 64 (each CTA 128 x 64): measured
-        c.kb = 0.25;                         // slower than one CTA per 128 x 64 tile
-        c.tile_store = 0.7;
-        c.partial = 1.5;
-        c.reduce_per_slot = 1.0;
-    } else if (path == 4) {  // CTA pair, 256 x 128 (each CTA 128 x 128): measured no faster
-        c.kb = 0.31;         // per k-block than one CTA per 128 x 128 tile
-        c.tile_store = 1.3;
-        c.partial = 3.0;
-        c.reduce_per_slot = 2.0;
     } else if (path == 2 && mma_n >= 256) {
         c.kb = 0.37;
         c.tile_store = 2.5;
@@ -74,7 +59,7 @@ static Costs costs_for(int32_t path, int32_t mma_n, int32_t stage_bytes) {
         c.reduce_per_slot = 2.0;
     }
     // the figures above are per 64 k-rows; stages of 128 k-rows cost twice
-    if ((path == 2 || path == 4) && mma_n < 256) c.kb *= 2.0;
+    if (path == 2 && mma_n < 256) c.kb *= 2.0;
     if (path == 3) {
         // swapped operands, streaming B: ~0.4 us per 18 KiB stage per SM
         c.kb = 0.40 * stage_bytes / 18432.0;
@@ -152,13 +137,12 @@ static void finish_split(gemm_relu_plan_t& p, int32_t grid, int32_t dp, int32_t 
     p.counter_count = (int64_t)sk * p.cluster;
 }
 
-// Fill the shape-dependent fields for one kernel shape.  `narrow_n` (path 3
-// only) is a C tile width of at most 64 columns, else 0 for 128.
-static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path,
-                       int32_t mma_n, int32_t narrow_n = 0, bool long_stages = false) {
+// Fill the shape-dependent fields for one kernel shape: path 2 with
+// mma_n = 64, 128 or 256; path 3 (mma_n = M padded to 16, tiles of 128
+// columns); path 4 (CTA pairs, mma_n = 256).
+static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int32_t path, int32_t mma_n) {
     p.path = path;
     p.mma_n = mma_n;
-    p.mcast = 1;
     p.cluster = (path == 4) ? 2 : 1;
     p.mma_m = (path == 4) ? 256 : 128;
     if (path == 2) {
@@ -169,34 +153,27 @@ static void shape_plan(gemm_relu_plan_t& p, int64_t M, int64_t N, int64_t K, int
         p.tile_n = mma_n;
     } else {
         p.tile_m = mma_n;  // padded M
-        p.tile_n = narrow_n > 0 ? narrow_n : 128;
+        p.tile_n = 128;
     }
     p.tiles_m = (int32_t)((M + p.tile_m - 1) / p.tile_m);
     p.tiles_n = (int32_t)((N + p.tile_n - 1) / p.tile_n);
     p.num_tiles = p.tiles_m * p.tiles_n;
     // k-rows per stage: 128, except 256-column tiles (tensor-bound already;
     // 64-row stages keep their ring deeper)
-    // (CTA pairs with 256-column tiles take 128-row stages when asked:
-    // ":bk128")
-    p.block_k = (mma_n == 256 && path != 3 && !(long_stages && path == 4)) ? kBlockK : 2 * kBlockK;
+    p.block_k = (mma_n == 256 && path != 3) ? kBlockK : 2 * kBlockK;
     p.num_kb = (int32_t)((K + p.block_k - 1) / p.block_k);
     p.group_m = p.tiles_m < 8 ? p.tiles_m : 8;
     // per CTA: columns of the MMA B operand it loads (half of the tile for
     // a pair; the padded rows of A when swapped)
     const int32_t b_cols = (path == 4) ? mma_n / 2 : mma_n;
     const int32_t b_bytes = b_cols * p.block_k * 2;
-    // MMA A operand per stage: 128 rows, or for the swapped kernel one
-    // 64-wide chunk of B columns per 64 tile columns (a narrow tile, at most
-    // 64 columns, takes one chunk and an M = 64 MMA)
-    const bool narrow = (path == 3 && p.tile_n <= 64);
-    const int32_t a_region = (path == 3) ? (narrow ? 1 : 2) * p.block_k * kSwizzleRowBytes : 128 * p.block_k * 2;
+    // MMA A operand per stage: 128 rows, or for the swapped kernel the
+    // tile's two 64-wide chunks of B columns
+    const int32_t a_region = 128 * p.block_k * 2;
     // bytes the TMA copies of one stage deliver
-    const int32_t a_box_bytes = (path == 3) ? (narrow ? p.tile_n : 128) * p.block_k * 2 : 128 * p.block_k * 2;
-    p.stage_bytes = a_box_bytes + b_bytes;
-    // B region: a pair CTA's (K, N) chunks are 64 columns wide, the last
-    // one possibly partial (256 x 192 tiles: 96 columns = 1.5 chunks)
-    const int32_t b_region = (path == 4) ? ((b_cols + 63) / 64) * 64 * p.block_k * 2
-                                         : ((b_bytes + 1023) / 1024) * 1024;
+    p.stage_bytes = a_region + b_bytes;
+    // B region (1 KiB aligned: the swizzle atoms)
+    const int32_t b_region = ((b_bytes + 1023) / 1024) * 1024;
     const int32_t stride = a_region + b_region;
     // tiled paths: C staging for the TMA stores; swapped: the buffer a
     // cluster split-K peer pushes its fp32 partial into (128 x mma_n)
@@ -308,7 +285,6 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         K > GEMM_RELU_MAX_DIM || num_sms < 1)
         return GEMM_ERR_INVALID_ARG;
     memset(plan, 0, sizeof(*plan));
-    plan->mcast = 1;
     if (M == 0 || N == 0) {
         plan->path = 0;
         return GEMM_OK;
@@ -325,10 +301,7 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     const char* f = force ? force : "";
     const bool dp_only = contains(f, ":dp");
     const bool force_csk = contains(f, ":c2");
-    const bool force_sk = contains(f, ":sk") && !contains(f, ":skt");
-    const bool long_stages = contains(f, ":bk128");
-    // ":skt": full waves but the last data-parallel, the rest stream-K
-    const bool force_sk_tail = contains(f, ":skt");
+    const bool force_sk = contains(f, ":sk");
     int32_t force_tail = 0;  // ":tS": full waves data-parallel, leftover tiles split S ways
     for (const char* q = f; *q; ++q)
         if (q[0] == ':' && q[1] == 't' && q[2] >= '0' && q[2] <= '9') force_tail = q[2] - '0';
@@ -348,32 +321,22 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     // for 32 < M <= 64 only where it splits K without stream-K (below);
     // else, and above, the 128 x 128 tiled kernel measured faster
     bool want_swap = M <= 64, want_t256 = M > 128, want_t128 = M > 32, want_pair = M > 128 && pairs > 0;
-    bool want_pair128 = want_pair, want_t64 = want_t128, want_pair192 = want_pair, want_pair64 = false;
+    bool want_t64 = want_t128;
     const bool swap_only = M <= 32 || starts_with(f, "swap");
     if (starts_with(f, "swap") && M <= 128) {
-        want_t256 = want_t128 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
+        want_t256 = want_t128 = want_pair = want_t64 = false;
         want_swap = true;
     } else if (starts_with(f, "tiled256")) {
-        want_swap = want_t128 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
+        want_swap = want_t128 = want_pair = want_t64 = false;
         want_t256 = true;
     } else if (starts_with(f, "tiled64")) {
-        want_swap = want_t256 = want_t128 = want_pair = want_pair128 = want_pair192 = false;
+        want_swap = want_t256 = want_t128 = want_pair = false;
         want_t64 = true;
     } else if (starts_with(f, "tiled128")) {
-        want_swap = want_t256 = want_pair = want_pair128 = want_t64 = want_pair192 = false;
+        want_swap = want_t256 = want_pair = want_t64 = false;
         want_t128 = true;
-    } else if (starts_with(f, "pair64") && pairs > 0) {
-        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair128 = want_pair192 = false;
-        want_pair64 = true;
-    } else if (starts_with(f, "pair192") && pairs > 0) {
-        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair128 = false;
-        want_pair192 = true;
-    } else if (starts_with(f, "pair128") && pairs > 0) {
-        want_swap = want_t256 = want_t128 = want_pair = want_t64 = want_pair192 = false;
-        want_pair128 = true;
     } else if (starts_with(f, "pair") && pairs > 0) {
-        want_pair128 = want_t64 = want_pair192 = false;
-        want_swap = want_t256 = want_t128 = false;
+        want_swap = want_t256 = want_t128 = want_t64 = false;
         want_pair = true;
     }
 
@@ -381,18 +344,12 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     auto take = [&](int32_t path, int32_t mma_n, int32_t workers) {
         gemm_relu_plan_t q;
         memset(&q, 0, sizeof(q));
-        shape_plan(q, M, N, K, path, mma_n, 0, long_stages);
+        shape_plan(q, M, N, K, path, mma_n);
         double cost = choose_split(q, workers, dp_only, force_splits, operands_fit_l2, pairs);
         if (force_tail > 1 && q.num_tiles >= workers && q.num_tiles % workers != 0) {
             q.cluster = (path == 4) ? 2 : 1;
             const int32_t sp = force_tail < q.num_kb ? force_tail : q.num_kb;
             finish_split(q, workers, (q.num_tiles / workers) * workers, q.num_tiles % workers, sp);
-            cost = 0.0;
-        }
-        if (force_sk_tail && q.num_tiles > workers && q.num_tiles % workers != 0) {
-            q.cluster = (path == 4) ? 2 : 1;
-            const int32_t full = q.num_tiles / workers;
-            finish_split(q, workers, (full - 1) * workers, q.num_tiles - (full - 1) * workers);
             cost = 0.0;
         }
         if (force_sk) {
@@ -417,23 +374,6 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         // small M: C^T = B^T A^T, so N runs along the 128-wide MMA M side
         // and M (padded to 16) is the MMA N side.
         const int32_t mpad = (int32_t)((M + 15) / 16) * 16;
-        // Narrow data-parallel tiles (8..64 columns, one TMA box per
-        // k-block) are only used when forced with "swapnW" (W = width):
-        // streaming B in strips narrower than 128 columns measured well
-        // below the bandwidth of 128-wide tiles split along K.
-        int32_t narrow = 0;
-        if (starts_with(f, "swapn"))
-            for (const char* d = f + 5; *d >= '0' && *d <= '9'; ++d) narrow = narrow * 10 + (*d - '0');
-        const bool use_narrow = narrow >= 8 && narrow <= 64 && narrow % 8 == 0;
-        if (use_narrow) {
-            gemm_relu_plan_t q;
-            memset(&q, 0, sizeof(q));
-            shape_plan(q, M, N, K, 3, mpad, narrow);
-            gemm_relu_plan_t r = q;
-            finish_split(r, q.num_tiles < num_sms ? q.num_tiles : num_sms, q.num_tiles, 0);
-            *plan = r;
-            return GEMM_OK;
-        }
         // Streaming B: cut each 128-column tile into S equal K ranges with
         // S = SMs / tiles (tile-fastest item order, so CTAs running together
         // sweep whole rows of B), when that keeps >= 3/4 of the SMs busy;
@@ -463,34 +403,10 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
         }
         if (swap_only) take(3, mpad, num_sms);
     }
-    // (packing is decided after the kernel shape, below)
     if (want_pair) take(4, 256, pairs);
-    if (want_pair128) take(4, 128, pairs);
-    if (want_pair192) take(4, 192, pairs);
-    if (want_pair64) take(4, 64, pairs);
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
     if (want_t64) take(2, 64, num_sms);
-    // An operand row pitch that is not a multiple of 128 bytes makes every
-    // 128-byte TMA box row straddle two L2 lines (on 3000 x 5000 x 2056 the
-    // L2 served 1.8 sectors per request instead of 3.9, and the GEMM took
-    // 57.5 us against 46.5 for 3072 x 5120 x 2048).  Copying the operands to
-    // a 128-byte pitch first measured slower all the same (59.8 us; the copy
-    // moves 66 MB), so it is only done when forced (":pk").  (The swapped
-    // kernel streams B once: a copy would triple its traffic.)
-    plan->pack = 0;
-    if (contains(f, ":pk") && !contains(f, ":npk") && (plan->path == 2 || plan->path == 4)) plan->pack = 1;
-    // A multicast: two CTAs of a cluster take the two tiles of a column
-    // pair; each fetches one of the two 64-k boxes of every A stage and the
-    // TMA writes it into both (so each SM requests 3/4 (128 x 64 tiles) or
-    // 2/3 (128 x 128) of the bytes it consumes).  Data-parallel plans of
-    // the one-CTA kernel with 128-row stages and an even number of tile
-    // columns and of CTAs.
-    plan->mcast = 1;
-    if (contains(f, ":mc") && plan->path == 2 && (plan->mma_n == 64 || plan->mma_n == 128) &&
-        plan->block_k == 2 * kBlockK && plan->cluster == 1 && plan->splits <= 1 && plan->sk_tiles == 0 &&
-        plan->dp_tiles == plan->num_tiles && plan->tiles_n % 2 == 0 && plan->grid % 2 == 0 && pairs > 0)
-        plan->mcast = 2;
     return GEMM_OK;
 }
 
@@ -512,45 +428,39 @@ int plan_boxes(const gemm_relu_plan_t& pl, int64_t M, int64_t N, int64_t K, bool
     const bool allow3d = !(force && strstr(force, ":no3d"));
     // A: 64 k by 128 rows (the padded rows of A when swapped) per 64-k
     // block; one 3-D copy of a stage's two blocks when K is a multiple of 64
-    // (the 2-D A boxes of the multicast kernel stay)
     o->a_box[0] = kBlockK;
     o->a_box[1] = swap ? (uint32_t)pl.tile_m : 128u;
     o->a_box[2] = 1;
-    if (allow3d && sub == 2 && K % kBlockK == 0 && pl.mcast <= 1) {
+    if (allow3d && sub == 2 && K % kBlockK == 0) {
         o->a_3d = 1;
         o->a_box[2] = sub;
     }
     if (!b_nk) {
-        // B (K, N): 64-column boxes of a stage's k-rows (a narrow swapped
-        // tile: one box of its width); a pair CTA whose columns end in a
-        // partial chunk (256 x 192: 96 columns) loads it through the second
-        // map with narrower boxes
-        o->b_box[0] = (swap && pl.tile_n <= 64) ? (uint32_t)pl.tile_n : 64u;
+        // B (K, N): 64-column boxes of a stage's k-rows, the second map's
+        // boxes the same
+        o->b_box[0] = 64u;
         o->b_box[1] = bk;
         o->b_box[2] = 1;
-        const uint32_t rem = pair ? (uint32_t)(pl.mma_n / 2) % 64u : 0u;
-        o->b2_box[0] = rem ? rem : o->b_box[0];
+        o->b2_box[0] = 64u;
         o->b2_box[1] = bk;
         // all of a CTA's whole chunks in one 3-D copy (two or more); with N
         // not a multiple of 64 the view covers the whole chunks, and a CTA
         // reaching the partial one uses the second (2-D) map
         const uint32_t cols = swap ? 128u : (pair ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
-        if (allow3d && (!swap || pl.tile_n == 128) && N >= 64 && cols % 64 == 0 && cols >= 128) {
+        if (allow3d && N >= 64 && cols % 64 == 0 && cols >= 128) {
             o->b_3d = 1;
-            o->b_box[0] = 64;
             o->b_box[2] = cols / 64;
             o->b_view_inner = (N / 64) * 64;
         }
     } else {
         // B (N, K): 64 k by the rows of N one CTA loads per stage
-        const uint32_t rows = swap ? (pl.tile_n <= 64 ? (uint32_t)pl.tile_n : 128u)
-                                   : (pair ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
+        const uint32_t rows = swap ? 128u : (pair ? (uint32_t)pl.mma_n / 2 : (uint32_t)pl.mma_n);
         o->b_box[0] = kBlockK;
         o->b_box[1] = rows;
         o->b_box[2] = 1;
         o->b2_box[0] = kBlockK;
         o->b2_box[1] = rows;
-        if (allow3d && (!swap || pl.tile_n == 128) && sub == 2 && K % kBlockK == 0) {
+        if (allow3d && sub == 2 && K % kBlockK == 0) {
             o->b_3d = 1;
             o->b_box[2] = sub;
         }

@@ -64,18 +64,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
-// tma_load_2d whose box is written, at the same shared-memory offset, into
-// every CTA of `cta_mask` in the cluster, each copy completing `bar` at that
-// offset in its own CTA.
-__device__ __forceinline__ void tma_load_2d_mcast(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                                  int32_t x, int32_t y, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // L2 policy that marks lines as the first to evict: for an operand that
 // every CTA together reads exactly once, so that it does not push reused
 // data out of L2.
@@ -378,16 +366,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar, uint16_t cta_mask = 1) 
             " [%0], %1;" ::"r"(bar),
             "h"(cta_mask)
             : "memory");
-}
-
-// One-CTA MMAs: arrive (once) on `bar` in every CTA of `cta_mask` when
-// every tcgen05 op issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit_mcast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives

@@ -34,20 +34,14 @@ constexpr int kBlockK = 64;  // k-block: 64 fp16 = one 128-byte swizzle row
 // Rasterisation: tiles are numbered so that a group of `group_m` tile rows
 // is walked column by column; CTAs running at the same time then share A
 // row-panels and B column-panels in L2.
-// (cols: the number of tile columns walked, p.tiles_n, or half of it for
-// column pairs)
-GR_HD void tile_coords_cols(const gemm_relu_plan_t& p, int32_t t, int32_t cols, int32_t& tm, int32_t& tn) {
-    const int32_t per_group = p.group_m * cols;
+GR_HD void tile_coords(const gemm_relu_plan_t& p, int32_t t, int32_t& tm, int32_t& tn) {
+    const int32_t per_group = p.group_m * p.tiles_n;
     const int32_t g = t / per_group;
     const int32_t first_m = g * p.group_m;
     const int32_t rows = (p.tiles_m - first_m) < p.group_m ? (p.tiles_m - first_m) : p.group_m;
     const int32_t r = t - g * per_group;
     tm = first_m + r % rows;
     tn = r / rows;
-}
-
-GR_HD void tile_coords(const gemm_relu_plan_t& p, int32_t t, int32_t& tm, int32_t& tn) {
-    tile_coords_cols(p, t, p.tiles_n, tm, tn);
 }
 
 // First stream-K unit of CTA c (c may equal grid: one past the end).
@@ -126,15 +120,7 @@ struct WorkIter {
                 w.nslots = 1;
             }
             ++dp_i;
-            if (p.mcast > 1) {
-                // A-multicast clusters: tiles 2j and 2j+1 (CTAs 2q and 2q+1 of
-                // one cluster, the grid being even) are the two columns of
-                // column pair j, rasterised like tiles
-                tile_coords_cols(p, w.tile >> 1, p.tiles_n >> 1, w.tm, w.tn);
-                w.tn = 2 * w.tn + (w.tile & 1);
-            } else {
-                tile_coords(p, w.tile, w.tm, w.tn);
-            }
+            tile_coords(p, w.tile, w.tm, w.tn);
             return true;
         }
         if (p.splits > 1) {
