@@ -540,21 +540,29 @@ def run_ours(args, w):
 
 
 def run_profile_launches(args, w):
-    """A few launches on one input set, for an ncu capture (no timing)."""
+    """A few launches on one input set, for an ncu capture (no timing).
+    --b-layout / --dtype select a gemm_relu_ex variant (B stored (N, K),
+    bfloat16 elements) on the same shape and value distribution."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
     from tiled_dense_gemm_gb300 import binding
-    from tiled_dense_gemm_gb300.workloads import workload_inputs
+    from tiled_dense_gemm_gb300.workloads import make_inputs
     device = torch.device("cuda", 0)
-    A, B = workload_inputs(w)
+    dt = torch.bfloat16 if args.dtype == "bf16" else torch.float16
+    A, B = make_inputs(w.M, w.N, w.K, w.seed, w.dist_a, w.scale_a, w.dist_b, w.scale_b,
+                       dtype=dt, b_layout=args.b_layout)
     a, b = A.to(device), B.to(device)
-    c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+    c = torch.empty((w.M, w.N), dtype=dt, device=device)
+    plain = args.b_layout == "kn" and args.dtype == "f16"
     for _ in range(args.ncu_launches):
-        binding.gemm_relu(a, b, c, True)
+        if plain:
+            binding.gemm_relu(a, b, c, True)
+        else:
+            binding.gemm_relu_ex(a, b, c, True, b_layout=args.b_layout)
     binding.check_device_error()
     torch.cuda.synchronize(device)
-    print(f"profile launches done: {args.ncu_launches} x {w.name}")
+    print(f"profile launches done: {args.ncu_launches} x {w.name} (B {args.b_layout}, {args.dtype})")
     return 0
 
 
@@ -571,6 +579,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling mode: run only this many launches of the workload and exit")
+    ap.add_argument("--b-layout", choices=["kn", "nk"], default="kn",
+                    help="profiling mode: B stored (K, N) or (N, K) (gemm_relu_ex)")
+    ap.add_argument("--dtype", choices=["f16", "bf16"], default="f16",
+                    help="profiling mode: element type (gemm_relu_ex)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
