@@ -98,11 +98,20 @@ int gemm_relu_ex(const void* A, const void* B, void* C,
 
 /*
  * Same operation on HOST buffers: copies A and B to library-owned device
- * buffers (one cudaMemcpyAsync each), runs gemm_relu on `stream`, copies C
- * back, and synchronizes `stream` before returning.  Pinned host memory
- * gives the fastest copies; pageable memory also works.  Alignment rules on
- * the host pointers are waived (the device copies are aligned); K % 8 and
- * N % 8 still apply.  Returns the device error status of the call as well.
+ * buffers, runs the GEMM, copies C back, and synchronizes `stream` before
+ * returning.  Small problems run as one block on `stream`.  Problems of at
+ * least 16 MiB (A, B and C together) with M >= 1024 run in up to 8 row
+ * blocks (multiples of 256 rows, at least 512) pipelined over two internal
+ * streams of the library: B and each block of A are copied in on one,
+ * block i's GEMM runs on `stream` once its rows are in, and its rows of C
+ * are copied out on the other, so the copy in of block i + 1, the GEMM of
+ * block i and the copy out of block i - 1 overlap.  All of it starts after
+ * the work already queued on `stream`.  (The environment variable
+ * GEMM_RELU_HOST_BLOCK_ROWS=r, for tuning, sets the block height; 0 keeps
+ * one block.)  Pinned host memory gives the fastest copies; pageable
+ * memory also works.  Alignment rules on the host
+ * pointers are waived (the device copies are aligned); K % 8 and N % 8
+ * still apply.  Returns the device error status of the call as well.
  */
 int gemm_relu_host(const void* A_host, const void* B_host, void* C_host,
                    int64_t M, int64_t N, int64_t K, int apply_relu, void* stream);

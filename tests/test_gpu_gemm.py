@@ -234,6 +234,23 @@ def test_host_buffer_entry_point():
     assert_close(C2, oracle.gemm_relu(A2, B2, False, threads=THREADS), "host entry point pageable")
 
 
+@pytest.mark.parametrize("name,relu,pinned", [("c3_4096", True, True), ("c5_ragged", False, True),
+                                              ("c5_ragged", True, False)])
+def test_host_buffer_entry_point_row_blocks(name, relu, pinned):
+    """Large problems go through the host-buffer entry point in row blocks
+    whose copies in, GEMMs and copies out overlap on three streams (4096^3:
+    8 blocks of 512 rows; 3000 rows: 5 blocks of 512 and one of 440):
+    every element, twice in a row, pinned and pageable host memory."""
+    A, B, ref = workload_and_ref(name, relu)
+    a, b = (A.pin_memory(), B.pin_memory()) if pinned else (A, B)
+    for _ in range(2):
+        C = torch.full(ref.shape, float("nan"), dtype=torch.float16)
+        C = C.pin_memory() if pinned else C
+        binding.gemm_relu_host(a, b, C, apply_relu=relu)
+        assert_close(C, ref, f"{name} host row blocks relu={relu} pinned={pinned}")
+        assert_relu_sign(C, relu)
+
+
 def test_stream_k_counters_are_left_zero():
     """Split tiles reset their arrival counters, so repeated calls stay correct."""
     A, B, ref = workload_and_ref("c4_skinny", True)

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libgemmrelu.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 
-SOURCES = ["gemm_relu.cu", "plan.cpp", "noalloc.cu"]
+SOURCES = ["gemm_relu.cu", "host_entry.cu", "plan.cpp", "noalloc.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
                 f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -1,5 +1,6 @@
 // C ABI of the GB300 gemm_relu library: argument checks, per-device state,
-// tensor-map encoding, workspace management and kernel launch.
+// tensor-map encoding, workspace management and kernel launch (the
+// host-buffer entry point is in host_entry.cu).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -13,6 +14,7 @@
 
 #include "gemm_kernel.cuh"
 #include "gemm_relu.h"
+#include "runtime.h"
 
 namespace gr {
 
@@ -23,33 +25,10 @@ __global__ void zero_fill_kernel(uint4* c, int64_t n16) {
         c[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-namespace {
+namespace rt {
 
-constexpr int kMaxDevices = 64;
-constexpr int kMaxDynSmem = 227 * 1024;  // sm_100-family opt-in limit per CTA
-
-struct StreamBuffers {
-    void* stream = nullptr;
-    float* ws = nullptr;  // stream-K partial tiles
-    size_t ws_bytes = 0;
-    uint32_t* counters = nullptr;  // split-K arrival counters + ready flags (zero between launches)
-    size_t counter_bytes = 0;
-    void* hA = nullptr;  // staging for the host-buffer entry point
-    void* hB = nullptr;
-    void* hC = nullptr;
-    size_t hA_bytes = 0, hB_bytes = 0, hC_bytes = 0;
-    int32_t* h_err = nullptr;  // pinned copy of the error word (host-buffer entry point)
-};
-
-struct DeviceState {
-    bool inited = false;
-    int status = GEMM_OK;
-    int sm_count = 0;
-    int max_pairs = 0;  // co-resident CTA pairs of the paired kernel
-    int32_t* d_err = nullptr;
-    bool attr_set[6] = {false, false, false, false, false, false};  // per kernel mode
-    std::vector<StreamBuffers> streams;
-};
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
 
 struct PlanKey {
     int64_t M, N, K;
@@ -64,8 +43,6 @@ struct PlanKeyHash {
     }
 };
 
-std::mutex g_mu;
-DeviceState g_dev[kMaxDevices];
 std::unordered_map<PlanKey, gemm_relu_plan_t, PlanKeyHash> g_plans[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -451,10 +428,11 @@ int reset_after_error_locked(DeviceState& d) {
     return GEMM_ERR_TIMEOUT;
 }
 
-}  // namespace
+}  // namespace rt
 }  // namespace gr
 
 using namespace gr;
+using namespace gr::rt;
 
 extern "C" int gemm_relu_ex(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                             int apply_relu, int b_layout, int dtype, void* stream) {
@@ -475,58 +453,6 @@ extern "C" int gemm_relu(const void* A, const void* B, void* C, int64_t M, int64
                          int apply_relu, void* stream) {
     return gemm_relu_ex(A, B, C, M, N, K, apply_relu, GEMM_B_KN, GEMM_DTYPE_F16, stream);
 }
-
-extern "C" int gemm_relu_host(const void* A_host, const void* B_host, void* C_host, int64_t M,
-                              int64_t N, int64_t K, int apply_relu, void* stream) {
-    int rc = check_args(A_host, B_host, C_host, M, N, K, false);
-    if (rc != GEMM_OK) return rc;
-    if (M == 0 || N == 0) return GEMM_OK;
-    int dev;
-    if ((rc = current_device(&dev)) != GEMM_OK) return rc;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    int32_t* h_err = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if ((rc = init_device_locked(dev)) != GEMM_OK) return rc;
-        DeviceState& d = g_dev[dev];
-        StreamBuffers& sb = buffers_for_locked(d, stream);
-        const size_t a_bytes = (size_t)M * K * 2, b_bytes = (size_t)K * N * 2, c_bytes = (size_t)M * N * 2;
-        if ((rc = grow(&sb.hA, &sb.hA_bytes, a_bytes > 16 ? a_bytes : 16, st, false)) != GEMM_OK) return rc;
-        if ((rc = grow(&sb.hB, &sb.hB_bytes, b_bytes > 16 ? b_bytes : 16, st, false)) != GEMM_OK) return rc;
-        if ((rc = grow(&sb.hC, &sb.hC_bytes, c_bytes, st, false)) != GEMM_OK) return rc;
-        if (a_bytes && cudaMemcpyAsync(sb.hA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        if (rc == GEMM_OK && b_bytes &&
-            cudaMemcpyAsync(sb.hB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        if (rc == GEMM_OK) rc = run_device(sb.hA, sb.hB, sb.hC, M, N, K, apply_relu, false, false, st, dev);
-        if (rc == GEMM_OK &&
-            cudaMemcpyAsync(C_host, sb.hC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        // the error word comes back in the same stream, so one synchronize
-        // covers the copies, the kernel and the check
-        if (rc == GEMM_OK && !sb.h_err && cudaHostAlloc(&sb.h_err, sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess) {
-            sb.h_err = nullptr;
-            rc = GEMM_ERR_OUT_OF_MEMORY;
-        }
-        if (rc == GEMM_OK &&
-            cudaMemcpyAsync(sb.h_err, d.d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-            rc = GEMM_ERR_CUDA;
-        if (rc != GEMM_OK) {
-            cudaGetLastError();
-            return rc;
-        }
-        h_err = sb.h_err;
-    }
-    if (cudaStreamSynchronize(st) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    if (*(volatile int32_t*)h_err == 0) return GEMM_OK;
-    std::lock_guard<std::mutex> lock(g_mu);
-    return reset_after_error_locked(g_dev[dev]);
-}
-
 
 extern "C" int gemm_relu_check_device_error(void* stream) {
     int dev;
@@ -582,6 +508,7 @@ extern "C" void gemm_relu_shutdown(void) {
                 cudaFree(s.hB);
                 cudaFree(s.hC);
                 if (s.h_err) cudaFreeHost(s.h_err);
+                pipe_release(s);
             }
             cudaFree(d.d_err);
         }
