@@ -227,6 +227,9 @@ typedef struct {
     int32_t stage_bytes; /* bytes of A and B tile per ring stage */
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
     int32_t tmem_cols;   /* tensor-memory columns allocated per CTA */
+    int32_t pack_a;      /* 1: A is first copied to a row pitch that is a multiple of 128 bytes (library
+                            workspace), because neither A's nor B's pitch is (decided here for B stored
+                            (K, N); B stored (N, K) shares A's pitch) */
     int64_t workspace_bytes; /* fp32 partial tiles for the stream-K tiles */
     int64_t counter_count;   /* arrival counters (one per split tile and CTA of a worker); the
                                 counter array also holds max_slots ready flags per counter */
@@ -248,7 +251,8 @@ typedef struct {
  * 256-row tile), by ":sk" to run every tile stream-K over all workers, or
  * by ":tS" for full data-parallel waves with the leftover tiles cut into S
  * K ranges; ":no3d" keeps every TMA copy two-dimensional (one copy per
- * 64-k block or 64-column chunk).
+ * 64-k block or 64-column chunk); ":pk" / ":npk" force the copy of A to a
+ * 128-byte pitch on (when K % 64 != 0) or off.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for bad sizes / null plan.
  */
 int gemm_relu_plan(int64_t M, int64_t N, int64_t K, int num_sms, gemm_relu_plan_t* plan);

@@ -74,7 +74,7 @@ SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), (48, 61
           (8, 4864, 1024), (16, 1000, 1024)]
 FORCES = ["", "tiled256", "tiled128", "pair", "tiled256:dp", "swap", "swap:dp", "swap:c2", "tiled128:c2",
           "swap:s7", "tiled128:s3", "pair:s5", "swap:sk", "tiled64", "tiled64:c2", "tiled128:no3d", "pair:no3d",
-          "swap:no3d", "tiled256:c2", "pair:t2"]
+          "swap:no3d", "tiled256:c2", "pair:t2", "pair:pk", "tiled128:pk"]
 
 
 @pytest.mark.parametrize("force", FORCES)

@@ -87,13 +87,15 @@ def test_workload_full_parity(name):
 
 
 @pytest.mark.parametrize("force", ["pair:t2", "pair:t3", "pair:t4", "tiled256:t2", "tiled128:t3", "pair:dp",
-                                   "pair:sk", "tiled128"])
+                                   "pair:sk", "tiled128", "pair:npk", "tiled256:pk"])
 def test_ragged_other_schedules_full(monkeypatch, force):
     """Other decompositions of the ragged workload -- full waves
     data-parallel with the leftover tiles split along K in 2-4 slots (the
     tail wave), data-parallel only, stream-K over all workers, one CTA per
-    128 x 128 tile -- on every output element, ReLU on and off; the split-K
-    counters are left at zero for the next call."""
+    128 x 128 tile, without the in-launch copy of A to a 128-byte pitch
+    (":npk"; the planner's plan makes it) and with it on one-CTA tiles
+    (":pk") -- on every output element, ReLU on and off; the split-K and
+    copy counters are left at zero for the next call."""
     monkeypatch.setenv("GEMM_RELU_FORCE_PATH", force)
     for relu in (True, False):
         A, B, ref = workload_and_ref("c5_ragged", relu)
@@ -273,7 +275,8 @@ FORCED_SHAPES = [(1, 8, 8), (129, 136, 72), (300, 264, 2056), (513, 520, 1000), 
                                    "tiled128:c2", "tiled256:c2", "swap:c2", "swap:sk", "tiled128:sk",
                                    "tiled64", "tiled64:s3", "tiled64:c2", "tiled128:s2", "pair:s2",
                                    "pair:s4", "tiled256:s2", "tiled64:s2", "tiled128:no3d", "pair:no3d",
-                                   "swap:no3d", "tiled256:no3d", "pair:t2"])
+                                   "swap:no3d", "tiled256:no3d", "pair:t2", "pair:pk", "tiled128:pk",
+                                   "pair:s3:pk", "tiled64:c2:pk"])
 def test_each_kernel_shape_parity(monkeypatch, force):
     """Every kernel shape (one CTA per 128 x 256 / 128 x 128 / 128 x 64
     tile, 256 x 256 CTA pairs, swapped operands), with and without stream-K,

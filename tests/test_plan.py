@@ -58,6 +58,11 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     assert d["num_kb"] == (K + d["block_k"] - 1) // d["block_k"]
     assert 2 <= d["num_stages"] <= 16
     assert d["smem_bytes"] <= SMEM_LIMIT
+    # A is copied to a 128-byte pitch only when neither pitch is aligned
+    assert d["pack_a"] in (0, 1)
+    if d["pack_a"]:
+        assert d["path"] in (2, 4) and K % 64 != 0
+        assert forced or (d["path"] == 4 and N % 64 != 0 and d["tiles_n"] >= 4)
     assert d["tmem_cols"] in (32, 64, 128, 256, 512) and d["tmem_cols"] >= 2 * d["mma_n"]
     assert 1 <= d["grid"] * d["cluster"] <= sms
     assert d["dp_tiles"] + d["sk_tiles"] == d["num_tiles"]
@@ -159,6 +164,20 @@ def test_tail_wave_split(gemm_lib, monkeypatch, force, sp):
         if T % workers:
             assert d["dp_tiles"] == (T // workers) * workers
             assert d["sk_tiles"] == T % workers and d["splits"] == sp and d["max_slots"] == sp
+
+
+def test_copy_of_a_decision(gemm_lib, monkeypatch):
+    monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
+    assert gemm_lib.plan(3000, 5000, 2056, 152).pack_a == 1      # both pitches misaligned
+    assert gemm_lib.plan(3000, 5120, 2056, 152).pack_a == 0      # B's pitch aligned
+    assert gemm_lib.plan(3000, 5000, 2048, 152).pack_a == 0      # A's pitch aligned
+    assert gemm_lib.plan(4096, 4096, 4096, 152).pack_a == 0
+    assert gemm_lib.plan(16, 8192, 8200, 152).pack_a == 0        # swapped operands
+    assert gemm_lib.plan(300, 264, 2056, 152).pack_a == 0        # A read by too few tiles
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "tiled128:pk")
+    assert gemm_lib.plan(300, 264, 2056, 152).pack_a == 1
+    monkeypatch.setenv("GEMM_RELU_FORCE_PATH", "pair:npk")
+    assert gemm_lib.plan(3000, 5000, 2056, 152).pack_a == 0
 
 
 def test_random_shapes(gemm_lib):

@@ -33,7 +33,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "path", "mma_m", "mma_n", "tile_m", "tile_n", "tiles_m", "tiles_n", "num_tiles",
         "num_kb", "block_k", "group_m", "grid", "cluster", "dp_tiles", "sk_tiles", "sk_q", "sk_r",
-        "splits", "max_slots", "num_stages", "stage_bytes", "smem_bytes", "tmem_cols")] + [
+        "splits", "max_slots", "num_stages", "stage_bytes", "smem_bytes", "tmem_cols", "pack_a")] + [
         ("workspace_bytes", ctypes.c_int64), ("counter_count", ctypes.c_int64)]
 
     def as_dict(self) -> dict:

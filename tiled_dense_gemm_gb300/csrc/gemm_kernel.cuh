@@ -94,6 +94,20 @@ struct KParams {
     // wait for that stage runs out; the host pairs it with a short
     // timeout_ns and a plan without clusters.
     int32_t test_drop_kb;
+    // A copied to a 128-byte row pitch inside the launch (plans with
+    // pack_a, when neither operand's row pitch is a multiple of 128 bytes):
+    // before its first tile, each CTA's epilogue warps copy their share of
+    // A's rows to pack_dst and count the CTA on pack_sync[0]; the producer
+    // of A's copies waits until every CTA has counted itself before the
+    // first copy of its second work item, and from then on reads A through
+    // the second map of A.  pack_sync[1] counts CTAs that have finished the
+    // launch; the last one resets both words.  pack_sync null: no copy.
+    const uint4* pack_src;
+    uint4* pack_dst;
+    int64_t pack_rows;
+    int64_t pack_dst_pitch;  // 16-byte vectors
+    int32_t pack_row_vecs;   // 16-byte vectors of a row of A
+    uint32_t* pack_sync;
     uint16_t* C;          // 16-bit words of C (binary16 or bfloat16)
     float* ws;            // stream-K partial tiles: [sk_tile][slot][col][128 lanes]
     uint32_t* counters;   // stream-K arrivals, one per stream-K tile, zero between launches
@@ -195,6 +209,7 @@ struct Producer {
     // second map of B (K, N): 64-column 2-D boxes, for the columns a 3-D
     // map of whole chunks leaves out
     const CUtensorMap* tmB2;
+    const CUtensorMap* tmA2;  // A at its 128-byte pitch (see KParams::pack_sync)
     gemm_relu_plan_t pl;
     uint32_t stages, stride, a_bytes, rank, S, full0, empty0, tx_bytes;
     WorkIter wi;
@@ -217,8 +232,10 @@ struct Producer {
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
                                         uint32_t a_bytes_, const CUtensorMap* tmA_, const CUtensorMap* tmB_,
-                                        const CUtensorMap* tmB2_, int32_t worker, uint32_t rank_, int32_t part_ = 0)
-        : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), tmB2(tmB2_), pl(p_.plan), stages(stages_), stride(stride_),
+                                        const CUtensorMap* tmB2_, const CUtensorMap* tmA2_, int32_t worker,
+                                        uint32_t rank_, int32_t part_ = 0)
+        : p(p_), ctrl(ctrl_), tmA(tmA_), tmB(tmB_), tmB2(tmB2_), tmA2(tmA2_), pl(p_.plan), stages(stages_),
+          stride(stride_),
           a_bytes(a_bytes_), rank(rank_), have_item(false), armed(false), kb(0), a_row(0), b_col(0), s(0), ph(0) {
         S = (uint32_t)pl.num_stages;
         full0 = smem_u32(&ctrl->full[0]);
@@ -433,11 +450,36 @@ struct Producer {
         }
     }
 
+    // Bounded wait until every CTA has copied its share of A to the
+    // 128-byte pitch; then A's copies switch to that copy.
+    __device__ __forceinline__ bool wait_packed() {
+        volatile uint32_t* arrived = p.pack_sync;
+        if (*arrived < gridDim.x) {
+            volatile int32_t* abort_flag = &ctrl->abort_flag;
+            const uint64_t t0 = globaltimer_ns();
+            while (*arrived < gridDim.x) {
+                if (*abort_flag) return false;
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    *abort_flag = 1;
+                    atomicCAS(p.err, 0, kErrProducer);
+                    return false;
+                }
+            }
+        }
+        __threadfence();
+        fence_proxy_async_global();  // the other CTAs' stores, before this thread's TMA reads
+        tmA = tmA2;
+        return true;
+    }
+
     template <bool kPre>
     __device__ __forceinline__ bool run(int32_t budget) {
         while (budget != 0) {
             if (!have_item || kb == w.kb1) {
                 if (!next_item()) return true;
+                if constexpr (!kPre && !T::kSwap) {
+                    if (items == 2 && part != 2 && p.pack_sync && !wait_packed()) return false;
+                }
             }
             if constexpr (!kPre) {
                 if (!armed) {
@@ -652,6 +694,36 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
     WorkItem w;
     uint32_t local = 0;
     float v[kChunk];
+
+    if constexpr (!T::kSwap) {
+        if (p.pack_sync) {
+            // this CTA's share of the copy of A to a 128-byte pitch: rows
+            // blockIdx.x * 4 + quarter, then every 4 * gridDim.x rows; one
+            // warp per row at a time, eight 16-byte loads in flight per lane
+            const int64_t nw = (int64_t)gridDim.x * 4;
+            for (int64_t r = (int64_t)blockIdx.x * 4 + quarter; r < p.pack_rows; r += nw) {
+                const uint4* src = p.pack_src + r * p.pack_row_vecs;
+                uint4* dst = p.pack_dst + r * p.pack_dst_pitch;
+                for (int32_t c0 = 0; c0 < p.pack_row_vecs; c0 += 8 * 32) {
+                    uint4 q[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int32_t c = c0 + u * 32 + (int32_t)lane;
+                        if (c < p.pack_row_vecs) q[u] = __ldcs(src + c);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int32_t c = c0 + u * 32 + (int32_t)lane;
+                        if (c < p.pack_row_vecs) dst[c] = q[u];
+                    }
+                }
+            }
+            fence_proxy_async_global();  // before other CTAs' TMA reads of these rows
+            __threadfence();
+            named_bar_sync(kEpiBarrier, kEpiThreads);
+            if (threadIdx.x == 64) atomicAdd(p.pack_sync, 1u);
+        }
+    }
 
     // where chunk c of this thread's lane goes
     auto sink = [&](const WorkItem& it, uint32_t c) {
@@ -1095,6 +1167,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmC,
+                     const __grid_constant__ CUtensorMap tmA2,
                      const __grid_constant__ KParams p) {
     using T = ModeTraits<kMode>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1179,7 +1252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B's.  The set-up (parameters, first work item) touches no
             // global memory, so it runs before the wait too; only the copies
             // come after it.
-            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank,
+            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, &tmA2, worker, rank,
                                  warp == 0 ? 1 : 2);
             prod.prime();
             grid_dependency_wait();
@@ -1194,7 +1267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Producer::prefetch).  (The tiled kernels measured faster
             // without: their prefetches hold up the first copies in the TMA
             // unit.)
-            Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, worker, rank);
+            Producer<kMode> pre(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, &tmA2, worker, rank);
             pre.prefetch(2 * pl.num_stages);
         }
         // (the MMA thread waits inside its role, after its set-up)
@@ -1230,6 +1303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc<T::kCG>(tmem_base, (uint32_t)pl.tmem_cols);
+    }
+    if (p.pack_sync && threadIdx.x == 0) {
+        // every role of this CTA is done (its producer is past its wait for
+        // the copy of A): the last CTA to get here resets both words for
+        // the next launch
+        if (atomicAdd(p.pack_sync + 1, 1u) == gridDim.x - 1) {
+            p.pack_sync[0] = 0u;
+            p.pack_sync[1] = 0u;
+        }
     }
 }
 

@@ -153,9 +153,9 @@ int grow(void** buf, size_t* have, size_t need, cudaStream_t stream, bool zero) 
 }
 
 int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool bf16) {
+              uint32_t box_outer, bool bf16, uint64_t pitch_elems = 0) {
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 2};  // bytes between rows
+    cuuint64_t strides[1] = {(pitch_elems ? pitch_elems : inner) * 2};  // bytes between rows
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
@@ -189,7 +189,8 @@ int encode_3d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer,
 
 template <int kMode>
 int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, const CUtensorMap& ta,
-                const CUtensorMap& tb, const CUtensorMap& tb2, const CUtensorMap& tc, cudaStream_t st) {
+                const CUtensorMap& tb, const CUtensorMap& tb2, const CUtensorMap& tc, const CUtensorMap& ta2,
+                cudaStream_t st) {
     auto fn = gemm_relu_kernel<kMode>;
     if (!d.attr_set[kMode]) {
         if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem) !=
@@ -222,7 +223,7 @@ int launch_mode(DeviceState& d, const gemm_relu_plan_t& pl, const KParams& kp, c
     }
     cfg.attrs = attr;
     cfg.numAttrs = n_attr;
-    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tb2, tc, kp) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, fn, ta, tb, tb2, tc, ta2, kp) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
@@ -245,14 +246,15 @@ int check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N
     return GEMM_OK;
 }
 
-// The tensor maps of one call: A, B (and B's second, 2-D map), C.
+// The tensor maps of one call: A, B (and B's second, 2-D map), C, and A's
+// copy at a 128-byte pitch (pack_a plans; else a copy of A's map).
 struct Maps {
-    CUtensorMap ta, tb, tb2, tc;
+    CUtensorMap ta, tb, tb2, tc, ta2;
     int32_t a3d, b3d;
 };
 
 int encode_maps(const gemm_relu_plan_t& pl, const void* A, const void* B, void* C, int64_t M, int64_t N,
-                int64_t K, bool b_nk, bool bf16, const char* force, Maps* m) {
+                int64_t K, bool b_nk, bool bf16, const char* force, const void* A2, uint64_t a2_pitch, Maps* m) {
     // the boxes of one stage's copies (3-D where the shapes allow)
     gemm_relu_boxes_t bx;
     int rc = plan_boxes(pl, M, N, K, b_nk, force, &bx);
@@ -262,6 +264,14 @@ int encode_maps(const gemm_relu_plan_t& pl, const void* A, const void* B, void* 
     else
         rc = encode_2d(&m->ta, A, (uint64_t)K, (uint64_t)M, bx.a_box[0], bx.a_box[1], bf16);
     if (rc != GEMM_OK) return rc;
+    if (A2) {
+        // (a pack_a plan has K % 64 != 0, so A's copies are 2-D)
+        if (bx.a_3d) return GEMM_ERR_INVALID_ARG;
+        rc = encode_2d(&m->ta2, A2, (uint64_t)K, (uint64_t)M, bx.a_box[0], bx.a_box[1], bf16, a2_pitch);
+        if (rc != GEMM_OK) return rc;
+    } else {
+        m->ta2 = m->ta;
+    }
     m->a3d = bx.a_3d;
     if (!b_nk) {
         // the second map: 64-column 2-D boxes (the partial chunk a 3-D view
@@ -296,10 +306,12 @@ struct MapKey {
     const void* A;
     const void* B;
     const void* C;
+    const void* A2;  // A's copy at a 128-byte pitch, or null
     int64_t M, N, K;
     int32_t flags;
     bool operator==(const MapKey& o) const {
-        return A == o.A && B == o.B && C == o.C && M == o.M && N == o.N && K == o.K && flags == o.flags;
+        return A == o.A && B == o.B && C == o.C && A2 == o.A2 && M == o.M && N == o.N && K == o.K &&
+               flags == o.flags;
     }
 };
 struct MapKeyHash {
@@ -307,6 +319,7 @@ struct MapKeyHash {
         uint64_t h = (uint64_t)(uintptr_t)k.A * 0x9E3779B97F4A7C15ull;
         h ^= (uint64_t)(uintptr_t)k.B + 0x7F4A7C159E3779B9ull + (h << 6) + (h >> 2);
         h ^= (uint64_t)(uintptr_t)k.C + 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)(uintptr_t)k.A2 + 0x2545F4914F6CDD1Dull + (h << 6) + (h >> 2);
         h ^= (uint64_t)k.M + 0xBF58476D1CE4E5B9ull + (h << 6) + (h >> 2);
         h ^= (uint64_t)k.N + 0x94D049BB133111EBull + (h << 6) + (h >> 2);
         h ^= (uint64_t)k.K + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
@@ -385,17 +398,37 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
         kp.ws = sb.ws;
         kp.counters = sb.counters;
     }
+    // Neither A's nor B's row pitch a multiple of 128 bytes: the launch
+    // also copies A to a 128-byte pitch (KParams::pack_sync) when the plan
+    // says it pays
+    void* A2 = nullptr;
+    uint64_t a2_pitch = 0;  // elements
+    if (pack_a_pays(pl, M, N, K, b_nk, forced ? force : nullptr)) {
+        a2_pitch = ((uint64_t)K + 63) / 64 * 64;
+        StreamBuffers& sb = buffers_for_locked(d, st);
+        int rc = grow(&sb.packed, &sb.packed_bytes, (size_t)M * a2_pitch * 2, st, false);
+        if (rc != GEMM_OK) return rc;
+        rc = grow(reinterpret_cast<void**>(&sb.pack_sync), &sb.pack_sync_bytes, 2 * sizeof(uint32_t), st, true);
+        if (rc != GEMM_OK) return rc;
+        A2 = sb.packed;
+        kp.pack_src = reinterpret_cast<const uint4*>(A);
+        kp.pack_dst = reinterpret_cast<uint4*>(A2);
+        kp.pack_rows = M;
+        kp.pack_row_vecs = (int32_t)(K / 8);
+        kp.pack_dst_pitch = (int64_t)(a2_pitch / 8);
+        kp.pack_sync = sb.pack_sync;
+    }
     Maps local;
     const Maps* m = &local;
     if (forced) {
-        int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, force, &local);
+        int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, force, A2, a2_pitch, &local);
         if (rc != GEMM_OK) return rc;
     } else {
         auto& cache = g_maps[dev];
-        const MapKey key{A, B, C, M, N, K, (b_nk ? 1 : 0) | (bf16 ? 2 : 0)};
+        const MapKey key{A, B, C, A2, M, N, K, (b_nk ? 1 : 0) | (bf16 ? 2 : 0)};
         auto it = cache.find(key);
         if (it == cache.end()) {
-            int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, nullptr, &local);
+            int rc = encode_maps(pl, A, B, C, M, N, K, b_nk, bf16, nullptr, A2, a2_pitch, &local);
             if (rc != GEMM_OK) return rc;
             if (cache.size() >= kMapCacheEntries) cache.clear();
             it = cache.emplace(key, local).first;
@@ -407,13 +440,13 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
     if (pl.path == 3) {
         // M = 128 tile columns; B^T is MN-major when B is stored (K, N)
         kp.idesc = make_idesc_f16_f32(128u, (uint32_t)pl.mma_n, /*a_mn=*/!b_nk, /*b_mn=*/false, bf16);
-        return launch_mode<2>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
+        return launch_mode<2>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, m->ta2, st);
     }
     kp.idesc = make_idesc_f16_f32((uint32_t)pl.mma_m, (uint32_t)pl.mma_n, /*a_mn=*/false, /*b_mn=*/!b_nk, bf16);
-    if (pl.path == 4) return launch_mode<3>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
-    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
-    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
-    return launch_mode<1>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, st);
+    if (pl.path == 4) return launch_mode<3>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, m->ta2, st);
+    if (pl.mma_n == 256) return launch_mode<0>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, m->ta2, st);
+    if (pl.mma_n == 64) return launch_mode<5>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, m->ta2, st);
+    return launch_mode<1>(d, pl, kp, m->ta, m->tb, m->tb2, m->tc, m->ta2, st);
 }
 
 // A launch gave up part-way (the error word is set): clear it and every
@@ -421,8 +454,10 @@ int run_device(const void* A, const void* B, void* C, int64_t M, int64_t N, int6
 int reset_after_error_locked(DeviceState& d) {
     cudaDeviceSynchronize();
     cudaMemset(d.d_err, 0, 16);
-    for (auto& s : d.streams)
+    for (auto& s : d.streams) {
         if (s.counters) cudaMemset(s.counters, 0, s.counter_bytes);
+        if (s.pack_sync) cudaMemset(s.pack_sync, 0, s.pack_sync_bytes);
+    }
     cudaDeviceSynchronize();
     cudaGetLastError();
     return GEMM_ERR_TIMEOUT;
@@ -504,6 +539,8 @@ extern "C" void gemm_relu_shutdown(void) {
             for (auto& s : d.streams) {
                 cudaFree(s.ws);
                 cudaFree(s.counters);
+                cudaFree(s.packed);
+                cudaFree(s.pack_sync);
                 cudaFree(s.hA);
                 cudaFree(s.hB);
                 cudaFree(s.hC);

@@ -184,7 +184,7 @@ extern "C" int gemm_relu_noalloc(const void* A, const void* B, void* C, int64_t 
     if ((rc = encode(&tb, B, (uint64_t)N, (uint64_t)K, 64u, (uint32_t)pl.block_k)) != GEMM_OK) return rc;
     if ((rc = encode(&tc, C, (uint64_t)N, (uint64_t)M, 64, 32)) != GEMM_OK) return rc;  // unused by this kernel
 
-    gemm_relu_kernel<2><<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, tb, tc, kp);
+    gemm_relu_kernel<2><<<pl.grid, kThreads, pl.smem_bytes, st>>>(ta, tb, tb, tc, ta, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }

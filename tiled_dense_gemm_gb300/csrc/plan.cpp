@@ -407,7 +407,23 @@ int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, co
     if (want_t256) take(2, 256, num_sms);
     if (want_t128) take(2, 128, num_sms);
     if (want_t64) take(2, 64, num_sms);
+    plan->pack_a = pack_a_pays(*plan, M, N, K, false, f) ? 1 : 0;
     return GEMM_OK;
+}
+
+// A row pitch that is not a multiple of 128 bytes makes every 128-byte TMA
+// box row straddle two L2 lines.  One such operand costs the tiled kernels
+// little; both together cost much more (3000 x 5000 x 2056: 56.5 us against
+// 48.0 with only A's pitch misaligned and 47.8 with only B's).  So when
+// both pitches are misaligned and A is reused by several tile columns,
+// A is copied to a 128-byte pitch first (a copy of 2 MK bytes each way).
+bool pack_a_pays(const gemm_relu_plan_t& pl, int64_t M, int64_t N, int64_t K, bool b_nk, const char* force) {
+    if (pl.path != 2 && pl.path != 4) return false;
+    if (K % 64 == 0) return false;  // A's pitch is aligned already
+    if (force && strstr(force, ":npk")) return false;
+    if (force && strstr(force, ":pk")) return true;
+    const bool b_misaligned = b_nk ? true : (N % 64 != 0);
+    return b_misaligned && pl.path == 4 && pl.tiles_n >= 4 && 2.0 * (double)M * (double)K >= 4.0 * 1024 * 1024;
 }
 
 }  // namespace gr

@@ -25,6 +25,10 @@ struct StreamBuffers {
     size_t ws_bytes = 0;
     uint32_t* counters = nullptr;  // split-K arrival counters + ready flags (zero between launches)
     size_t counter_bytes = 0;
+    void* packed = nullptr;  // A copied to a 128-byte row pitch (pack_a plans)
+    size_t packed_bytes = 0;
+    uint32_t* pack_sync = nullptr;  // the two counters of that copy (zero between launches)
+    size_t pack_sync_bytes = 0;
     void* hA = nullptr;  // staging for the host-buffer entry point
     void* hB = nullptr;
     void* hC = nullptr;

@@ -166,6 +166,12 @@ struct WorkIter {
 int plan_problem(int64_t M, int64_t N, int64_t K, int num_sms, int max_pairs, const char* force,
                  gemm_relu_plan_t* plan);
 
+// Whether A is first copied to a row pitch that is a multiple of 128 bytes
+// (the plan's pack_a, decided for B stored (K, N), refined here for B
+// stored (N, K)); `force` ":pk" / ":npk" forces it on (when K % 64 != 0) or
+// off.  Defined in plan.cpp.
+bool pack_a_pays(const gemm_relu_plan_t& plan, int64_t M, int64_t N, int64_t K, bool b_nk, const char* force);
+
 // The TMA boxes of one ring stage's copies under `plan` (3-D where the
 // shapes allow, unless `force` holds ":no3d").  Defined in plan.cpp.
 int plan_boxes(const gemm_relu_plan_t& plan, int64_t M, int64_t N, int64_t K, bool b_nk, const char* force,
