@@ -255,6 +255,43 @@ def time_device(w, device, steps, warmup, world):
                                     "median": each[len(each) // 2] * 1e3}}
 
 
+def host_call_us(w, device, calls=400):
+    """Host time of one gemm_relu call (CPU timer around a run of calls
+    queued behind a device-side sleep, so no call waits for the GPU):
+    with the plan and tensor maps cached (the normal path), and with both
+    rebuilt on every call (the same plan forced through
+    GEMM_RELU_FORCE_PATH, which bypasses both caches)."""
+    import torch
+    from tiled_dense_gemm_gb300 import binding
+    from tiled_dense_gemm_gb300.workloads import workload_inputs
+    A, B = workload_inputs(w)
+    a, b = A.to(device), B.to(device)
+    c = torch.empty((w.M, w.N), dtype=torch.float16, device=device)
+    stream = torch.cuda.current_stream(device)
+    pl = binding.plan(w.M, w.N, w.K, torch.cuda.get_device_properties(device).multi_processor_count)
+    force = {(2, 64): "tiled64", (2, 128): "tiled128", (2, 256): "tiled256", (4, 256): "pair"}.get(
+        (pl.path, pl.mma_n), "swap")
+    out = {}
+    for label, env in (("cached", None), ("rebuilt", force)):
+        if env:
+            os.environ["GEMM_RELU_FORCE_PATH"] = env
+        try:
+            for _ in range(5):
+                binding.gemm_relu(a, b, c, True, stream)
+            torch.cuda.synchronize(device)
+            torch.cuda._sleep(int(calls * 40_000))  # keeps the device busy while the calls queue
+            t0 = time.perf_counter()
+            for _ in range(calls):
+                binding.gemm_relu(a, b, c, True, stream)
+            out[label] = (time.perf_counter() - t0) / calls * 1e6
+            torch.cuda.synchronize(device)
+        finally:
+            os.environ.pop("GEMM_RELU_FORCE_PATH", None)
+    binding.check_device_error(stream)
+    out["forced_plan"] = force
+    return out
+
+
 def time_hot_l2(w, device, steps):
     """The same input set every launch (operands may stay in L2): a labelled
     hot-L2 figure, not the headline."""
@@ -473,6 +510,8 @@ def run_ours(args, w):
                             "plan": {k: p2[k] for k in ("path", "mma_n", "grid", "cluster", "splits",
                                                         "sk_tiles")},
                             "steps": max(args.steps, 20)}
+            if name == "c1_256":
+                others[name]["host_us_per_call"] = host_call_us(wo, device)
             if name == "c4_skinny":
                 hot = time_hot_l2(wo, device, max(args.steps, 20))
                 others[name]["hot_l2"] = {
