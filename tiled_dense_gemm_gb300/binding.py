@@ -145,6 +145,16 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _on_device(device, fn, *args):
+    """Call fn(*args) with `device` current (no device switch when it
+    already is: the switch costs more host time than the call itself)."""
+    import torch
+    if device.index is None or device.index == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
 def gemm_relu(a, b, c=None, apply_relu: bool = True, stream=None):
     """C = ReLU(a @ b) (or a @ b) for CUDA fp16 tensors a (M, K), b (K, N).
 
@@ -168,9 +178,8 @@ def gemm_relu(a, b, c=None, apply_relu: bool = True, stream=None):
     elif (c.dtype != torch.float16 or tuple(c.shape) != (M, N) or c.device != a.device
           or not c.is_contiguous()):
         raise ValueError("c must be a contiguous float16 (M, N) tensor on a's device")
-    with torch.cuda.device(a.device):
-        rc = lib().gemm_relu(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
-                             int(bool(apply_relu)), _stream_handle(stream, a.device))
+    rc = _on_device(a.device, lib().gemm_relu, a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                    int(bool(apply_relu)), _stream_handle(stream, a.device))
     if rc != GEMM_OK:
         raise GemmReluError(rc, "gemm_relu")
     return c
@@ -206,10 +215,9 @@ def gemm_relu_ex(a, b, c=None, apply_relu: bool = True, b_layout: str = "kn", st
     elif (c.dtype != a.dtype or tuple(c.shape) != (M, N) or c.device != a.device
           or not c.is_contiguous()):
         raise ValueError("c must be a contiguous (M, N) tensor of a's type on a's device")
-    with torch.cuda.device(a.device):
-        rc = lib().gemm_relu_ex(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
-                                int(bool(apply_relu)), B_LAYOUTS[b_layout], dtypes[a.dtype],
-                                _stream_handle(stream, a.device))
+    rc = _on_device(a.device, lib().gemm_relu_ex, a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                    int(bool(apply_relu)), B_LAYOUTS[b_layout], dtypes[a.dtype],
+                    _stream_handle(stream, a.device))
     if rc != GEMM_OK:
         raise GemmReluError(rc, "gemm_relu_ex")
     return c
@@ -269,9 +277,8 @@ def gemm_relu_noalloc(a, b, c, apply_relu: bool = True, stream=None):
         raise ValueError("a, b and c must be contiguous row-major")
     M, K = a.shape
     N = b.shape[1]
-    with torch.cuda.device(a.device):
-        rc = lib().gemm_relu_noalloc(a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
-                                     int(bool(apply_relu)), _stream_handle(stream, a.device))
+    rc = _on_device(a.device, lib().gemm_relu_noalloc, a.data_ptr(), b.data_ptr(), c.data_ptr(), M, N, K,
+                    int(bool(apply_relu)), _stream_handle(stream, a.device))
     if rc != GEMM_OK:
         raise GemmReluError(rc, "gemm_relu_noalloc")
     return c
