@@ -92,8 +92,12 @@ static double estimate(const gemm_relu_plan_t& p, const Costs& c) {
             t += (double)(w.kb1 - w.kb0) * c.kb;
             if (w.nslots == 1)
                 t += 0.25 * c.tile_store;
-            else if (shared)  // publish, read and store (S-1)/S, (S-1)/S and 1/S of the tile
-                t += (c.partial + c.reduce_per_slot) * (w.nslots - 1) / w.nslots + c.tile_store / w.nslots;
+            else if (shared)  // publish, read and store (S-1)/S, (S-1)/S and 1/S of the tile; the
+                              // split item runs first, so this overlaps the worker's next tile
+                              // when that tile's mainloop is long enough (measured: K = 2048
+                              // gains, K = 1024 loses)
+                t += (dp_n > 0 && (double)p.num_kb * c.kb >= 8.0 ? 0.25 : 1.0) *
+                     ((c.partial + c.reduce_per_slot) * (w.nslots - 1) / w.nslots + c.tile_store / w.nslots);
             else
                 t += c.partial + (w.slot == 0 ? w.nslots * c.reduce_per_slot + c.tile_store : 0.0);
         }
@@ -246,10 +250,9 @@ static double choose_split(gemm_relu_plan_t& p, int32_t workers, bool dp_only, i
                 for (int32_t sp = 2; sp <= 4 && sp <= p.num_kb; ++sp) {
                     gemm_relu_plan_t q = p;
                     finish_split(q, workers, full * workers, T % workers, sp);
-                    // (+1.5 us: the fixup's cost varies; take the split tail
-                    // only for a clear gain -- 2048 x 8192 x 2048 measured no
-                    // faster with an estimated 0.5 us gain)
-                    const double cost = estimate(q, c) + 1.5 + 1e-3 * (double)q.sk_tiles;
+                    // (+0.5 us: the fixup's cost varies; take the split tail
+                    // only for a clear gain)
+                    const double cost = estimate(q, c) + 0.5 + 1e-3 * (double)q.sk_tiles;
                     if (best_cost < 0.0 || cost < best_cost) {
                         best_cost = cost;
                         best = q;

@@ -104,41 +104,56 @@ struct WorkIter {
         }
     }
 
+    GR_HD bool next_dp(const gemm_relu_plan_t& p, WorkItem& w) {
+        if (dp_i >= dp_n) return false;
+        w.tile = cta + dp_i * p.grid;
+        w.sk_index = -1;
+        if (cluster_split(p)) {
+            w.kb0 = (int32_t)((int64_t)rank * p.num_kb / p.cluster);
+            w.kb1 = (int32_t)((int64_t)(rank + 1) * p.num_kb / p.cluster);
+            w.slot = rank;
+            w.nslots = p.cluster;
+        } else {
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.slot = 0;
+            w.nslots = 1;
+        }
+        ++dp_i;
+        tile_coords(p, w.tile, w.tm, w.tn);
+        return true;
+    }
+
+    GR_HD bool next_split(const gemm_relu_plan_t& p, WorkItem& w) {
+        if (u >= u1) return false;
+        // split item: tile fastest, so workers running together read the
+        // same K range of neighbouring tiles
+        const int32_t t = (int32_t)(u % p.sk_tiles);
+        const int32_t sp = (int32_t)(u / p.sk_tiles);
+        w.sk_index = t;
+        w.tile = p.dp_tiles + t;
+        w.kb0 = (int32_t)((int64_t)sp * p.num_kb / p.splits);
+        w.kb1 = (int32_t)((int64_t)(sp + 1) * p.num_kb / p.splits);
+        w.slot = sp;
+        w.nslots = p.splits;
+        u += p.grid;
+        tile_coords(p, w.tile, w.tm, w.tn);
+        return true;
+    }
+
+    // Items in the order a worker runs them: data-parallel tiles, then its
+    // split or stream-K share -- except when the slots of each split tile
+    // share its reduction (concurrent_split): then the split item comes
+    // first, so that all slots of a tile run together at the start and the
+    // reduction overlaps the worker's next tile (double-buffered TMEM)
+    // instead of adding to the end of the launch.
     GR_HD bool next(const gemm_relu_plan_t& p, WorkItem& w) {
-        if (dp_i < dp_n) {
-            w.tile = cta + dp_i * p.grid;
-            w.sk_index = -1;
-            if (cluster_split(p)) {
-                w.kb0 = (int32_t)((int64_t)rank * p.num_kb / p.cluster);
-                w.kb1 = (int32_t)((int64_t)(rank + 1) * p.num_kb / p.cluster);
-                w.slot = rank;
-                w.nslots = p.cluster;
-            } else {
-                w.kb0 = 0;
-                w.kb1 = p.num_kb;
-                w.slot = 0;
-                w.nslots = 1;
-            }
-            ++dp_i;
-            tile_coords(p, w.tile, w.tm, w.tn);
-            return true;
+        if (concurrent_split(p)) {
+            if (next_split(p, w)) return true;
+            return next_dp(p, w);
         }
-        if (p.splits > 1) {
-            if (u >= u1) return false;
-            // split item: tile fastest, so workers running together read
-            // the same K range of neighbouring tiles
-            const int32_t t = (int32_t)(u % p.sk_tiles);
-            const int32_t sp = (int32_t)(u / p.sk_tiles);
-            w.sk_index = t;
-            w.tile = p.dp_tiles + t;
-            w.kb0 = (int32_t)((int64_t)sp * p.num_kb / p.splits);
-            w.kb1 = (int32_t)((int64_t)(sp + 1) * p.num_kb / p.splits);
-            w.slot = sp;
-            w.nslots = p.splits;
-            u += p.grid;
-            tile_coords(p, w.tile, w.tm, w.tn);
-            return true;
-        }
+        if (next_dp(p, w)) return true;
+        if (p.splits > 1) return next_split(p, w);
         if (u < u1) {
             const int64_t t = u / p.num_kb;
             const int32_t kb0 = (int32_t)(u - t * p.num_kb);
