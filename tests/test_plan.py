@@ -166,6 +166,27 @@ def test_tail_wave_split(gemm_lib, monkeypatch, force, sp):
             assert d["sk_tiles"] == T % workers and d["splits"] == sp and d["max_slots"] == sp
 
 
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (3000, 5000, 2056), (8192, 8192, 2048)])
+def test_split_items_come_first_when_the_reduction_is_shared(gemm_lib, monkeypatch, shape):
+    """With a split tail whose slots share the reduction (every worker has
+    at most one split item, and the columns divide into whole epilogue
+    chunks per slot), each worker runs its split item first, so that all
+    slots of a split tile run together and the reduction overlaps the
+    worker's next tile."""
+    monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
+    p = gemm_lib.plan(*shape, 152)
+    d = p.as_dict()
+    assert d["splits"] > 1 and d["sk_tiles"] * d["splits"] <= d["grid"]
+    assert d["mma_n"] % (d["splits"] * 64) == 0
+    for w in range(d["grid"]):
+        items = gemm_lib.plan_work_items(p, w)
+        split = [i for i, it in enumerate(items) if it["nslots"] > 1]
+        if w < d["sk_tiles"] * d["splits"]:
+            assert split == [0], (w, items[:2])
+        else:
+            assert split == []
+
+
 def test_copy_of_a_decision(gemm_lib, monkeypatch):
     monkeypatch.delenv("GEMM_RELU_FORCE_PATH", raising=False)
     assert gemm_lib.plan(3000, 5000, 2056, 152).pack_a == 1      # both pitches misaligned
