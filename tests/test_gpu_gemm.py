@@ -175,6 +175,31 @@ def test_extreme_aspect_ratios(shape):
     assert_close(C, oracle.gemm_relu(A, B, True, threads=THREADS), str(shape))
 
 
+@pytest.mark.parametrize("shape", [(1 << 20, 4096, 64), (1 << 24, 8, 72)])
+def test_outputs_beyond_32_bit_element_offsets(shape):
+    """C with 2^32 elements (8 GiB; element offsets past 2^31) and a 2^24-row
+    problem (131072 row tiles): every row block is written, checked on the
+    first and last 128 rows and 64 random rows against the oracle, all
+    columns, and on a canary element past the end of C."""
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, seed=M % 997 + N + K, dist_a="uniform", dist_b="uniform")
+    a, b = A.to(DEV), B.to(DEV)
+    buf = torch.empty(M * N + 8, dtype=torch.float16, device=DEV)
+    buf[M * N:] = 7.0
+    c = buf[:M * N].view(M, N)
+    binding.gemm_relu(a, b, c)
+    binding.check_device_error()
+    assert (buf[M * N:] == 7.0).all(), "write past the end of C"
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([np.arange(128), np.arange(M - 128, M), rng.integers(0, M, 64)]))
+    idx = torch.from_numpy(rows).to(DEV)
+    got = c.index_select(0, idx).cpu()
+    ref = oracle.gemm_relu(A[torch.from_numpy(rows)].contiguous(), B, True, threads=THREADS)
+    assert_close(got, ref, f"{shape} sampled rows")
+    del buf, c
+    torch.cuda.empty_cache()
+
+
 def test_k_zero_writes_positive_zero():
     c = torch.full((37, 40), float("nan"), dtype=torch.float16, device=DEV)
     a = torch.empty((37, 0), dtype=torch.float16, device=DEV)
