@@ -70,6 +70,12 @@ struct __align__(8) Ctrl {
     uint32_t tmem_addr;
     int32_t abort_flag;
     int32_t last_flag;
+    // where the stage-arming producer stopped (next stage, its phase parity,
+    // whether the ring has wrapped) and how many fix_bar units the split-K
+    // fixup armed: what an aborting CTA waits for before its shared memory
+    // is released
+    int32_t ring_s, ring_ph, ring_lap;
+    int32_t fix_armed;
 };
 static_assert(sizeof(Ctrl) <= 1024, "control block exceeds its reserved 1 KiB");
 
@@ -228,6 +234,7 @@ struct Producer {
     bool b_edge;           // B (K, N), b3d: this item's columns reach past the 3-D map's whole chunks
     int32_t part;          // copies this thread issues: 0 all, 1 A's (and arms each stage), 2 B's
     int32_t items;         // work items begun
+    int32_t issued;        // stages armed and issued by run()
     int32_t drop_kb;       // test hook: k-block of the first item not copied (-1: none)
 
     __device__ __forceinline__ Producer(const KParams& p_, Ctrl* ctrl_, uint32_t stages_, uint32_t stride_,
@@ -252,6 +259,7 @@ struct Producer {
         b_edge = false;
         part = part_;
         items = 0;
+        issued = 0;
         drop_kb = p_.test_drop_kb - 1;
         pol_first = l2_policy_evict_first();
         wi.init(pl, worker, (int32_t)rank);
@@ -501,9 +509,20 @@ struct Producer {
                 ph ^= 1u;
             }
             ++kb;
+            if constexpr (!kPre) ++issued;
             if (budget > 0) --budget;
         }
         return true;
+    }
+
+    // Record where the stage-arming thread stopped (for the drain of an
+    // aborting CTA; a pair's stages are armed in its leader only).
+    __device__ __forceinline__ void save_ring() {
+        if (part != 2 && (!T::kPair || rank == 0)) {
+            ctrl->ring_s = (int32_t)s;
+            ctrl->ring_ph = (int32_t)ph;
+            ctrl->ring_lap = issued >= (int32_t)S ? 1 : 0;
+        }
     }
 };
 
@@ -1090,6 +1109,7 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
         }
         if (fast && threadIdx.x == 64) {
             fence_proxy_async_global();
+            ctrl->fix_armed = (int32_t)((ncols + 63u) / 64u);
             for (uint32_t u = 0; u * 64u < ncols; ++u) {
                 const uint32_t ub = (ncols - u * 64u < 64u ? ncols - u * 64u : 64u) * 512u;
                 mbar_arrive_expect_tx(smem_u32(&ctrl->fix_bar[u]), (uint32_t)(w.nslots - 1) * ub);
@@ -1163,6 +1183,26 @@ __device__ __forceinline__ void epilogue_role(const KParams& p, Ctrl* ctrl, uint
 
 // ------------------------------------------------------------------ kernel
 
+// Bounded wait (100 us in all) for the copies an aborting CTA issued: the
+// full barrier of every ring stage armed in the current lap (parity
+// ring_ph) and, once the ring has wrapped, in the previous one (the other
+// parity), and the fixup's bulk-copy barriers.
+__device__ __forceinline__ void drain_copies(Ctrl* ctrl, uint32_t S) {
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = 100000ull;
+    const uint32_t ring_s = (uint32_t)ctrl->ring_s, ring_ph = (uint32_t)ctrl->ring_ph;
+    const bool lap = ctrl->ring_lap != 0;
+    for (uint32_t i = 0; i < S; ++i) {
+        if (i >= ring_s && !lap) continue;  // never armed
+        const uint32_t parity = i < ring_s ? ring_ph : ring_ph ^ 1u;
+        while (!mbar_try_wait(smem_u32(&ctrl->full[i]), parity))
+            if (globaltimer_ns() - t0 > limit) return;
+    }
+    for (int32_t u = 0; u < ctrl->fix_armed; ++u)
+        while (!mbar_try_wait(smem_u32(&ctrl->fix_bar[u]), 0))
+            if (globaltimer_ns() - t0 > limit) return;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_relu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -1221,6 +1261,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&ctrl->peer_free), 1);
         ctrl->abort_flag = 0;
         ctrl->last_flag = 0;
+        ctrl->ring_s = 0;
+        ctrl->ring_ph = 0;
+        ctrl->ring_lap = 0;
+        ctrl->fix_armed = 0;
         fence_mbar_init();
 
         if (T::kSwap && cluster_split(pl) && rank == 0)
@@ -1257,6 +1301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prod.prime();
             grid_dependency_wait();
             prod.issue(-1);
+            prod.save_ring();
         }
         __syncwarp();
     } else {
@@ -1288,13 +1333,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_role<kMode>(p, ctrl, tmem_base, worker, rank, &tmC, stages, staging);
     }
 
-    if ((warp == 0 || warp == 6) && lane == 0 && *(volatile int32_t*)&ctrl->abort_flag) {
-        // aborting: give copies already issued time to land before the
-        // shared memory is released
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 100000ull) {
-        }
-    }
+    // Every role has returned, so the abort flag is final.  An aborting CTA
+    // waits (bounded) until the copies it issued into its ring stages and
+    // fixup buffers have landed -- each armed stage's full barrier completes
+    // its phase when its bytes arrive -- before its shared memory is
+    // released; a stage armed for bytes that were never issued ends the
+    // wait at the limit.
+    __syncthreads();
+    if (threadIdx.x == 0 && *(volatile int32_t*)&ctrl->abort_flag) drain_copies(ctrl, (uint32_t)pl.num_stages);
     tc_fence_before();
     if (clustered)
         cluster_sync_relaxed();  // a peer's shared memory may be read (MMA, DSMEM) until here
