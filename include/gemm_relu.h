@@ -217,7 +217,11 @@ typedef struct {
     int32_t grid;        /* persistent workers (a worker is `cluster` CTAs) */
     int32_t cluster;     /* CTAs per worker: 1, or 2 for path 4 */
     int32_t dp_tiles;    /* tiles [0, dp_tiles) are done whole, round-robin over CTAs */
-    int32_t sk_tiles;    /* tiles [dp_tiles, num_tiles) are split along K (stream-K) */
+    int32_t sk_tiles;    /* tiles [dp_tiles, num_tiles) are split along K (stream-K); when the
+                            slots of each split tile share its reduction (every worker has at
+                            most one split item, and the columns divide into whole epilogue
+                            chunks per slot) the split tiles are instead [0, sk_tiles), the
+                            whole ones after them, and each worker runs its split item first */
     int32_t sk_q, sk_r;  /* stream-K k-blocks per CTA: q, plus 1 for CTAs < r */
     int32_t splits;      /* > 1: tiles [dp_tiles, num_tiles) are instead cut into `splits`
                             equal K ranges; item i is (tile i % T, K range i / T), T the

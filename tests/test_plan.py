@@ -69,6 +69,13 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
     assert d["workspace_bytes"] == d["sk_tiles"] * d["cluster"] * d["max_slots"] * 128 * d["mma_n"] * 4
     assert d["counter_count"] == d["sk_tiles"] * d["cluster"]
 
+    # split tiles: the last sk_tiles in raster order, or the first ones when
+    # their slots share the reduction (their items then run first)
+    chunk = 16 if d["path"] == 3 else 64
+    concurrent = (d["splits"] > 1 and d["sk_tiles"] * d["splits"] <= d["grid"]
+                  and d["mma_n"] % (d["splits"] * chunk) == 0)
+    split_lo = 0 if concurrent else d["dp_tiles"]
+    split_hi = split_lo + d["sk_tiles"]
     cover = defaultdict(int)
     slots = defaultdict(dict)
     coords = {}
@@ -90,7 +97,7 @@ def _check(gemm_lib, M, N, K, sms, forced=False):
                 assert it["slot"] == r and it["nslots"] == d["cluster"]
                 assert it["kb0"] == r * d["num_kb"] // d["cluster"]
                 assert it["kb1"] == (r + 1) * d["num_kb"] // d["cluster"]
-            elif it["tile"] < d["dp_tiles"]:
+            elif not split_lo <= it["tile"] < split_hi:
                 assert (it["kb0"], it["kb1"], it["nslots"]) == (0, d["num_kb"], 1)
             else:
                 units += it["kb1"] - it["kb0"]

@@ -10,7 +10,13 @@
 //      (the first r CTAs take q+1).  A run may start or end inside a tile;
 //      the CTAs sharing a tile each own one "slot" of it, numbered in K
 //      order, and the last one to finish adds the slots' fp32 partial tiles
-//      in slot order (so the result does not depend on which CTA is last).
+//      in slot order (so the result does not depend on which CTA is last);
+//      or, with `splits` > 1, split tiles cut into `splits` equal K ranges,
+//      one item each.  When every worker has at most one such item and the
+//      columns divide into whole epilogue chunks per slot, the slots of a
+//      tile share its reduction (concurrent_split): the split tiles are
+//      then tiles [0, sk_tiles), the whole ones [sk_tiles, num_tiles), and
+//      each worker runs its split item first.
 // This generalises the split-KV decode idea of the TileLang MLA example
 // ("Writing High-Performance Kernels in TileLang", MLA section: spread a
 // long reduction over idle SMs and combine the pieces) to the K dimension
@@ -106,7 +112,9 @@ struct WorkIter {
 
     GR_HD bool next_dp(const gemm_relu_plan_t& p, WorkItem& w) {
         if (dp_i >= dp_n) return false;
-        w.tile = cta + dp_i * p.grid;
+        // (with the split items first, the split tiles also come first in
+        // the raster order, so that the first round's tiles are neighbours)
+        w.tile = (concurrent_split(p) ? p.sk_tiles : 0) + cta + dp_i * p.grid;
         w.sk_index = -1;
         if (cluster_split(p)) {
             w.kb0 = (int32_t)((int64_t)rank * p.num_kb / p.cluster);
@@ -131,7 +139,7 @@ struct WorkIter {
         const int32_t t = (int32_t)(u % p.sk_tiles);
         const int32_t sp = (int32_t)(u / p.sk_tiles);
         w.sk_index = t;
-        w.tile = p.dp_tiles + t;
+        w.tile = concurrent_split(p) ? t : p.dp_tiles + t;
         w.kb0 = (int32_t)((int64_t)sp * p.num_kb / p.splits);
         w.kb1 = (int32_t)((int64_t)(sp + 1) * p.num_kb / p.splits);
         w.slot = sp;
