@@ -252,6 +252,55 @@ def test_side_stream_and_back_to_back_calls():
         assert_close(c.cpu(), ref, "side stream")
 
 
+def test_cuda_graph_capture_and_replay():
+    """After one call of each shape (which sizes the library's workspace),
+    gemm_relu can be captured in a CUDA graph: replays on new inputs give
+    the oracle's results (a split-tail plan with its fp32 workspace and
+    counters, and a small-M cluster split-K plan)."""
+    for name in ("c5_ragged", "c4_skinny"):
+        A, B, ref = workload_and_ref(name, True)
+        a, b = A.to(DEV), B.to(DEV)
+        c = torch.empty(ref.shape, dtype=torch.float16, device=DEV)
+        s = torch.cuda.Stream(DEV)
+        with torch.cuda.stream(s):
+            binding.gemm_relu(a, b, c, stream=s)  # warm-up outside the capture
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        a2, b2 = torch.zeros_like(a), torch.zeros_like(b)
+        with torch.cuda.graph(g, stream=s):
+            binding.gemm_relu(a2, b2, c, stream=torch.cuda.current_stream(DEV))
+        a2.copy_(a)
+        b2.copy_(b)
+        c.fill_(float("nan"))
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        binding.check_device_error()
+        assert_close(c.cpu(), ref, f"{name} graph replay")
+
+
+def test_two_streams_with_split_workspaces_at_once():
+    """Split-tail plans on two streams at the same time use separate
+    workspaces and counters: both results are the oracle's."""
+    A, B, ref = workload_and_ref("c3_4096", True)
+    a, b = A.to(DEV), B.to(DEV)
+    s1, s2 = torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)
+    c1 = torch.empty(ref.shape, dtype=torch.float16, device=DEV)
+    c2 = torch.empty(ref.shape, dtype=torch.float16, device=DEV)
+    for s, c in ((s1, c1), (s2, c2)):  # size each stream's workspace first
+        binding.gemm_relu(a, b, c, stream=s)
+    torch.cuda.synchronize()
+    c1.fill_(float("nan"))
+    c2.fill_(float("nan"))
+    for _ in range(3):
+        binding.gemm_relu(a, b, c1, stream=s1)
+        binding.gemm_relu(a, b, c2, stream=s2)
+    binding.check_device_error(s1)
+    binding.check_device_error(s2)
+    assert_close(c1.cpu(), ref, "stream 1")
+    assert_close(c2.cpu(), ref, "stream 2")
+
+
 def test_host_buffer_entry_point():
     A, B = workload_inputs("c4_skinny")
     C = binding.gemm_relu_host(A.pin_memory(), B.pin_memory())
