@@ -221,3 +221,17 @@ def within_tolerance(c_test, ref, rtol: float = 1e-2, atol: float = 1e-2) -> np.
     c_test = np.asarray(c_test, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     return np.abs(c_test - ref) <= atol + rtol * np.abs(ref)
+
+
+def matches_ieee(c_test, ref, rtol: float = 1e-2, atol: float = 1e-2) -> np.ndarray:
+    """Elementwise comparison that also covers non-finite results (inputs
+    holding NaN or infinities): a NaN expected value must be NaN, an
+    infinite one the same infinity, a finite one within_tolerance.  The
+    expected values follow the IEEE 754 rules (a NaN operand or 0 x inf
+    makes a NaN term, inf + (-inf) is NaN) and ReLU's x > 0 ? x : +0."""
+    c_test = np.asarray(c_test, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    fin = np.isfinite(ref)
+    with np.errstate(invalid="ignore"):
+        close = np.abs(np.where(fin, c_test, 0.0) - np.where(fin, ref, 0.0)) <= atol + rtol * np.abs(np.where(fin, ref, 0.0))
+    return np.where(np.isnan(ref), np.isnan(c_test), np.where(np.isinf(ref), c_test == ref, close & np.isfinite(c_test)))

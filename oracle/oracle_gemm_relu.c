@@ -28,7 +28,10 @@
  *   - accumulation is in binary64 (stronger than the pages' fp32), loop
  *     order i-k-j, so for every (i,j) the terms are added in k order;
  *   - ReLU maps -0.0 to +0.0 (max(x, 0) with the sign of zero dropped);
- *   - NaN/Inf inputs are not part of the contract (parity unpinned there).
+ *   - NaN/Inf inputs follow IEEE 754 binary64 arithmetic: a NaN operand or
+ *     inf x 0 gives a NaN term, inf + (-inf) is NaN, and ReLU's x > 0 ? x : 0
+ *     turns NaN and -inf into +0 (pinned in the CPU tests from the IEEE
+ *     rules applied term by term).
  */
 #include <stdint.h>
 #include <stddef.h>

@@ -19,7 +19,11 @@ What fixes the expected values, none of it the oracle's own code:
 * invariants: ReLU output non-negative with no -0; zero K-padding changes
   nothing; relu-off is odd in A and homogeneous in B; relu-on equals
   max(relu-off, 0); (A.B)^T equals B^T.A^T;
-* a float64 matmul from a library (torch CPU) within the binary64 bound.
+* a float64 matmul from a library (torch CPU) within the binary64 bound;
+* IEEE 754 rules for NaN and infinite operands (a NaN operand or 0 x inf
+  makes the product NaN, inf + (-inf) is NaN, a NaN term makes the sum
+  NaN), applied term by term with Python floats, and ReLU read as
+  x > 0 ? x : +0 (NaN and -inf become +0).
 """
 from __future__ import annotations
 
@@ -215,8 +219,80 @@ def pin_torch64(ref, seed=14, fmt=F16):
     return fails
 
 
+def ieee_expected(Ad, Bd, relu):
+    """Exact A.B for decoded inputs holding NaN / infinities, by the IEEE 754
+    rules applied to each term: NaN if a product is NaN (a NaN operand or
+    0 x inf) or the infinite products have both signs; the infinity of the
+    one sign present otherwise; else the exact rational sum.  ReLU: x > 0 ?
+    x : +0.  Returns float64 (finite sums rounded once)."""
+    M, K = Ad.shape
+    N = Bd.shape[1]
+    out = np.empty((M, N))
+    for i in range(M):
+        for j in range(N):
+            terms = [float(Ad[i, k]) * float(Bd[k, j]) for k in range(K)]
+            if any(t != t for t in terms):
+                v = float("nan")
+            elif any(t == float("inf") for t in terms) and any(t == float("-inf") for t in terms):
+                v = float("nan")
+            elif any(t == float("inf") for t in terms):
+                v = float("inf")
+            elif any(t == float("-inf") for t in terms):
+                v = float("-inf")
+            else:
+                v = float(sum((Fraction(float(Ad[i, k])) * Fraction(float(Bd[k, j])) for k in range(K)),
+                              Fraction(0)))
+            if relu:
+                v = v if v > 0 else 0.0
+            out[i, j] = v
+    return out
+
+
+def special_inputs(M, N, K, seed, fmt=F16):
+    """Finite random A, B (|x| < 2) with NaN and infinities planted so that
+    C holds every case: a NaN row and column, +inf rows and columns whose
+    other factor is positive, negative or zero, and dot products with
+    +inf and -inf terms (NaN)."""
+    rng = np.random.default_rng(seed)
+    A = rng.uniform(-2, 2, (M, K))
+    B = rng.uniform(-2, 2, (K, N))
+    B[rng.random((K, N)) < 0.15] = 0.0
+    inf, nan = float("inf"), float("nan")
+    A[0, K // 3] = nan
+    A[1 % M, 0] = inf
+    A[2 % M, K - 1] = -inf
+    A[3 % M, 1 % K], A[3 % M, K // 2] = inf, -inf
+    B[K // 4, 1 % N] = nan
+    B[(K - 1) // 2, 2 % N] = -inf
+    B[K - 1, 3 % N] = inf
+    return fmt.enc(A), fmt.enc(B)
+
+
+def pin_ieee_specials(ref, fmt=F16):
+    fails = []
+    for t, (M, N, K) in enumerate([(5, 6, 7), (4, 9, 16), (6, 4, 33)]):
+        A, B = special_inputs(M, N, K, seed=31 + t, fmt=fmt)
+        for relu in (True, False):
+            exp = ieee_expected(fmt.dec(A), fmt.dec(B), relu)
+            got = ref(A, B, relu)
+            same_nan = np.isnan(got) == np.isnan(exp)
+            fin = np.isfinite(exp)
+            same_inf = np.where(np.isinf(exp), got == exp, True)
+            close = np.where(fin, np.abs(np.where(fin, got, 0) - np.where(fin, exp, 0))
+                             <= 4 * _bound(np.where(np.isfinite(fmt.dec(A)), A, 0).astype(A.dtype),
+                                           np.where(np.isfinite(fmt.dec(B)), B, 0).astype(B.dtype), fmt)
+                             + 1e-300, True)
+            bad = ~(same_nan & same_inf & close)
+            if relu:
+                bad |= np.signbit(got) & (got == 0)
+            if bad.any():
+                i, j = np.argwhere(bad)[0]
+                fails.append(f"IEEE specials {M}x{N}x{K} relu={relu} [{i},{j}]: {got[i, j]} != {exp[i, j]}")
+    return fails
+
+
 ALL_PINS = [pin_golden, pin_bruteforce, pin_integer_exact, pin_identity, pin_ones,
-            pin_invariants, pin_torch64]
+            pin_invariants, pin_torch64, pin_ieee_specials]
 # the pins that take a ``fmt`` (the golden fixtures are binary16 values)
 FMT_PINS = [pin_bruteforce, pin_integer_exact, pin_identity, pin_ones, pin_invariants,
-            pin_torch64]
+            pin_torch64, pin_ieee_specials]

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 import oracle_pins as P
+from oracle import matches_ieee as oracle_matches
 
 
 def _real(oracle_mod):
@@ -128,6 +129,75 @@ def test_pins_catch_planted_mistake(oracle_mod, idx):
     mutant = _mutants(oracle_mod)[idx]
     caught = [pin.__name__ for pin in P.ALL_PINS if pin(mutant)]
     assert caught, f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def _special_mutants(oracle_mod):
+    """Plausible mistakes that only non-finite inputs show."""
+    g = oracle_mod.gemm_relu
+
+    def relu_passes_nan(A, B, r):  # max written as x < 0 ? 0 : x
+        off = g(A, B, False)
+        return np.where(off < 0, 0.0, off) if r else off
+
+    def nan_operands_dropped(A, B, r):
+        A2 = np.where(np.isnan(A.astype(np.float64)), 0, A).astype(A.dtype)
+        B2 = np.where(np.isnan(B.astype(np.float64)), 0, B).astype(B.dtype)
+        return g(A2, B2, r)
+
+    def zero_factor_terms_skipped(A, B, r):  # 0 x inf counted as 0
+        a = A.astype(np.float64)
+        b = B.astype(np.float64)
+        with np.errstate(invalid="ignore"):
+            t = a[:, :, None] * b[None, :, :]
+            t = np.where((a[:, :, None] == 0) | (b[None, :, :] == 0), 0.0, t)
+            off = t.sum(axis=1)
+        return np.where(off > 0, off, 0.0) if r else off
+
+    def infinity_saturated(A, B, r):  # a clamping cast instead of IEEE overflow
+        return np.clip(g(A, B, r), -oracle_mod.FP16_MAX, oracle_mod.FP16_MAX)
+
+    return [relu_passes_nan, nan_operands_dropped, zero_factor_terms_skipped, infinity_saturated]
+
+
+@pytest.mark.parametrize("idx", range(4))
+def test_pins_catch_planted_mistake_with_specials(oracle_mod, idx):
+    mutant = _special_mutants(oracle_mod)[idx]
+    caught = [pin.__name__ for pin in P.ALL_PINS if pin(mutant)]
+    assert caught, f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def test_specials_by_hand(oracle_mod):
+    """Small cases whose results follow from the IEEE 754 rules alone."""
+    inf, nan = float("inf"), float("nan")
+    h = np.float16
+    # a NaN operand: its row is NaN, +0 after ReLU
+    A = np.array([[1, nan], [2, 3]], h)
+    B = np.array([[1, 1], [1, 1]], h)
+    off = oracle_mod.gemm_relu(A, B, False)
+    assert np.isnan(off[0]).all() and off[1].tolist() == [5.0, 5.0]
+    on = oracle_mod.gemm_relu(A, B, True)
+    assert on[0].tolist() == [0.0, 0.0] and not np.signbit(on[0]).any()
+    # inf times a positive, a negative and a zero factor
+    A = np.array([[inf, 1]], h)
+    B = np.array([[1, -1, 0], [1, 1, 1]], h)
+    off = oracle_mod.gemm_relu(A, B, False)
+    assert off[0, 0] == inf and off[0, 1] == -inf and np.isnan(off[0, 2])
+    assert oracle_mod.gemm_relu(A, B, True)[0].tolist() == [inf, 0.0, 0.0]
+    # inf + (-inf) is NaN; inf + inf stays inf
+    assert np.isnan(oracle_mod.gemm_relu(np.array([[inf, -inf]], h), np.array([[1], [1]], h), False)[0, 0])
+    assert oracle_mod.gemm_relu(np.array([[inf, inf]], h), np.array([[1], [2]], h), False)[0, 0] == inf
+    # finite results beyond binary16's range stay finite (the oracle does not round)
+    big = oracle_mod.gemm_relu(np.array([[65504, 65504]], h), np.array([[65504], [65504]], h), True)
+    assert big[0, 0] == 2 * 65504.0 ** 2
+
+
+def test_matches_ieee_rule():
+    ref = np.array([np.nan, np.inf, -np.inf, 1.0, 0.0])
+    assert oracle_matches(np.array([np.nan, np.inf, -np.inf, 1.005, 0.0]), ref).all()
+    assert not oracle_matches(np.array([0.0, np.inf, -np.inf, 1.0, 0.0]), ref)[0]
+    assert not oracle_matches(np.array([np.nan, -np.inf, -np.inf, 1.0, 0.0]), ref)[1]
+    assert not oracle_matches(np.array([np.nan, np.inf, 65504.0, 1.0, 0.0]), ref)[2]
+    assert not oracle_matches(np.array([np.nan, np.inf, -np.inf, 1.03, np.nan]), ref)[3:].any()
 
 
 # ---- B stored (N, K) and bfloat16 elements (oracle_gemm_relu_ex) -----------
