@@ -334,6 +334,12 @@ struct Producer {
         return true;
     }
 
+    // The first work item, for a call ahead of the set-up barrier (parameters
+    // and arithmetic only).
+    __device__ __forceinline__ void first_item() {
+        if (!have_item) next_item();
+    }
+
     // Everything before the first copy, for a call ahead of the dependency
     // wait so that it overlaps the previous kernel: the first work item
     // (parameters and arithmetic) and the first stage's expected-bytes
@@ -1235,7 +1241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    if (warp == 0 && lane == 0) {
+    // Set-up: warp 2 (an epilogue warp, idle until the first accumulator)
+    // initialises the barriers, warp 1 allocates tensor memory, and the
+    // producer warps meanwhile build their state (below).
+    if (warp == 2 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if constexpr (!T::kSwap) tma_prefetch_desc(&tmC);
@@ -1276,28 +1285,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc<T::kCG>(smem_u32(&ctrl->tmem_addr), (uint32_t)pl.tmem_cols);
         tmem_relinquish<T::kCG>();
     }
-    tc_fence_before();
-    if (clustered)
-        cluster_sync();  // the peers' barriers are initialised before any remote arrive
-    else
-        __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = ctrl->tmem_addr;
-    // Everything above touches only this CTA's (or cluster's) on-chip state,
-    // so it may overlap the previous kernel of the stream; nothing below may
-    // read or write global memory before that kernel has completed.  The
-    // next kernel may start launching now: it waits the same way.
-    grid_launch_dependents();
+    // The set-up barrier.  Each warp reaches it once, from its own branch
+    // below (a warp-uniform barrier instruction in each).  Everything before
+    // it touches only this CTA's (or cluster's) on-chip state, so it may
+    // overlap the previous kernel of the stream; nothing after it may read
+    // or write global memory before that kernel has completed.  The next
+    // kernel may start launching once it is passed: it waits the same way.
+    auto setup_barrier = [&]() {
+        tc_fence_before();
+        if (clustered)
+            cluster_sync();  // the peers' barriers are initialised before any remote arrive
+        else
+            cta_barrier_sync();
+        tc_fence_after();
+        grid_launch_dependents();
+    };
     if (warp == 0 || warp == 6) {
+        // Two producer threads, one per operand: a single thread issues one
+        // TMA copy per ~250-450 cycles, so two in parallel stream faster.
+        // Warp 0 issues A's copies and arms each stage, warp 6 B's.  The
+        // whole warp builds the producer's state -- parameters and the first
+        // work item, no shared or global memory: ~1500 cycles of integer
+        // work -- during the set-up, before the barrier; lane 0 then arms
+        // the first stage, waits for the previous kernel and copies.
+        Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, &tmA2, worker, rank,
+                             warp == 0 ? 1 : 2);
+        prod.first_item();
+        setup_barrier();
         if (lane == 0) {
-            // Two producer threads, one per operand: a single thread issues
-            // one TMA copy per ~250-450 cycles, so two in parallel stream
-            // faster.  Warp 0 issues A's copies and arms each stage, warp 6
-            // B's.  The set-up (parameters, first work item) touches no
-            // global memory, so it runs before the wait too; only the copies
-            // come after it.
-            Producer<kMode> prod(p, ctrl, stages, stride, a_bytes, &tmA, &tmB, &tmB2, &tmA2, worker, rank,
-                                 warp == 0 ? 1 : 2);
             prod.prime();
             grid_dependency_wait();
             prod.issue(-1);
@@ -1305,6 +1320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
+        setup_barrier();
         if (T::kSwap && warp == 2 && lane == 0) {
             // Small M: warm L2 with the boxes of this CTA's first two rings
             // of k-blocks (B streams from DRAM) while the previous kernel
@@ -1319,6 +1335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp != 1) grid_dependency_wait();
     }
 
+    const uint32_t tmem_base = ctrl->tmem_addr;
     if (warp == 1) {
         if (lane == 0 && (!T::kPair || rank == 0)) {  // one thread (of a pair's leader) issues the MMAs
             mma_role<kMode>(p, ctrl, stages, stride, a_bytes, tmem_base, worker, rank);

@@ -204,6 +204,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 
 // All threads of every CTA in the cluster.
+// CTA-wide barrier 0 over all threads.  Unlike __syncthreads() it may be
+// reached from different (warp-uniform) branches, one instruction per warp.
+__device__ __forceinline__ void cta_barrier_sync() {
+    asm volatile("bar.sync 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                      "memory");

@@ -88,14 +88,21 @@ GR_HD bool cluster_split(const gemm_relu_plan_t& p) {
     return (p.path == 2 || p.path == 3) && p.cluster > 1;
 }
 
+// Integer division is a software routine on the GPU (a 64-bit one several
+// hundred cycles of dependent instructions), and these run before a CTA's
+// first copy: every quotient that fits in 32 bits is taken in 32 bits
+// (split items: u < sk_tiles * splits; k-block bounds: slot * num_kb with
+// slot <= 16 and num_kb < 2^25).
 struct WorkIter {
     int32_t cta;
     int32_t rank;  // CTA rank in the cluster (cluster split-K); 0 otherwise
     int32_t dp_i, dp_n;
     int64_t u, u1;  // stream-K units, or split items when p.splits > 1
+    bool cs;        // concurrent_split(p), taken once
 
     GR_HD void init(const gemm_relu_plan_t& p, int32_t c, int32_t r = 0) {
         cta = c;
+        cs = concurrent_split(p);
         rank = cluster_split(p) ? r : 0;
         dp_i = 0;
         dp_n = (c < p.dp_tiles) ? (p.dp_tiles - 1 - c) / p.grid + 1 : 0;
@@ -114,11 +121,11 @@ struct WorkIter {
         if (dp_i >= dp_n) return false;
         // (with the split items first, the split tiles also come first in
         // the raster order, so that the first round's tiles are neighbours)
-        w.tile = (concurrent_split(p) ? p.sk_tiles : 0) + cta + dp_i * p.grid;
+        w.tile = (cs ? p.sk_tiles : 0) + cta + dp_i * p.grid;
         w.sk_index = -1;
         if (cluster_split(p)) {
-            w.kb0 = (int32_t)((int64_t)rank * p.num_kb / p.cluster);
-            w.kb1 = (int32_t)((int64_t)(rank + 1) * p.num_kb / p.cluster);
+            w.kb0 = rank * p.num_kb / p.cluster;
+            w.kb1 = (rank + 1) * p.num_kb / p.cluster;
             w.slot = rank;
             w.nslots = p.cluster;
         } else {
@@ -136,12 +143,12 @@ struct WorkIter {
         if (u >= u1) return false;
         // split item: tile fastest, so workers running together read the
         // same K range of neighbouring tiles
-        const int32_t t = (int32_t)(u % p.sk_tiles);
-        const int32_t sp = (int32_t)(u / p.sk_tiles);
+        const int32_t sp = (int32_t)u / p.sk_tiles;
+        const int32_t t = (int32_t)u - sp * p.sk_tiles;
         w.sk_index = t;
-        w.tile = concurrent_split(p) ? t : p.dp_tiles + t;
-        w.kb0 = (int32_t)((int64_t)sp * p.num_kb / p.splits);
-        w.kb1 = (int32_t)((int64_t)(sp + 1) * p.num_kb / p.splits);
+        w.tile = cs ? t : p.dp_tiles + t;
+        w.kb0 = sp * p.num_kb / p.splits;
+        w.kb1 = (sp + 1) * p.num_kb / p.splits;
         w.slot = sp;
         w.nslots = p.splits;
         u += p.grid;
@@ -156,7 +163,7 @@ struct WorkIter {
     // reduction overlaps the worker's next tile (double-buffered TMEM)
     // instead of adding to the end of the launch.
     GR_HD bool next(const gemm_relu_plan_t& p, WorkItem& w) {
-        if (concurrent_split(p)) {
+        if (cs) {
             if (next_split(p, w)) return true;
             return next_dp(p, w);
         }
