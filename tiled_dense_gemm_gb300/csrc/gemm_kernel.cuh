@@ -13,6 +13,8 @@
 //               quarter of the accumulator), ReLU, round to fp16/bf16, store to
 //               C; or, for a tile split along K, store an fp32 partial and
 //               let the last CTA to finish sum the partials in slot order.
+//               (Warp 2 also initialises the barriers at set-up, while the
+//               producer warps build their state.)
 // B is read as stored: (K, N) row-major (an MN-major MMA operand) or
 // (N, K) row-major (K-major, C = ReLU(A . B^T)); the layout and the element
 // type are runtime flags that change only descriptors, copy coordinates and
