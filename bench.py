@@ -249,10 +249,21 @@ def time_device(w, device, steps, warmup, world):
     torch.cuda.synchronize(device)
     binding.check_device_error(stream)
     each = sorted(e0.elapsed_time(e1) for e0, e1 in evs)
+    # what an event pair with nothing between takes, queued the same way:
+    # part of every per-launch figure above
+    empty = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(n_each)]
+    torch.cuda._sleep(int(max(4_000_000, n_each * 200_000)))
+    for e0, e1 in empty:
+        e0.record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    alone = sorted(e0.elapsed_time(e1) for e0, e1 in empty)
     return {"total_ms": total, "launch_ms": total / steps, "sets": len(sets),
             "set_bytes": 2 * (w.M * w.K + w.K * w.N),
             "per_launch_event_us": {"launches": n_each, "min": each[0] * 1e3,
-                                    "median": each[len(each) // 2] * 1e3}}
+                                    "median": each[len(each) // 2] * 1e3,
+                                    "event_pair_alone_median": alone[len(alone) // 2] * 1e3}}
 
 
 def host_call_us(w, device, calls=400):
