@@ -54,6 +54,12 @@ typedef enum {
  *          tensor-memory-accelerator copies).  M has no constraint.
  *          M == 0 or N == 0: nothing is done.  K == 0: C is set to +0.
  *
+ * Arithmetic: fp32 accumulation of the exact binary16 products, ReLU as
+ * x > 0 ? x : +0 on the accumulator (so -0 and NaN become +0), then one
+ * round-to-nearest-even cast (results beyond 65504 become infinities).
+ * NaN and infinite inputs follow IEEE 754: a NaN operand or inf x 0 makes
+ * a NaN term, infinities of both signs in one sum give NaN.
+ *
  * Execution is asynchronous on `stream`; GEMM_OK means enqueued.  A device
  * fault of this call (e.g. a timed-out wait) is reported by the next
  * gemm_relu_check_device_error().  Shapes whose work is split along K use a
